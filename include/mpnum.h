@@ -1,0 +1,247 @@
+/*
+ * mpnum.h — C ABI of libmpnum.so, the GB300 (sm_103a) mixed-precision hot path.
+ *
+ * Three parts of the precision machinery around the GEMMs of mixed-precision
+ * training, each a stream-ordered call on one GPU:
+ *   1. the fused optimizer step: unscale, inf/NaN check, AdamW on FP32
+ *      masters, rounded 16-bit working copy, and the dynamic loss scale;
+ *   2. the FP8 delayed-scaling cast with its amax-history ring;
+ *   3. NVFP4 quantisation (E2M1 codes, E4M3 block scales, FP32 tensor scale,
+ *      1x16 or 16x16 blocks, optional random Hadamard transform, round to
+ *      nearest even or stochastic rounding), plus the standalone transform.
+ *
+ * Pages cited (title, then section):
+ *   [MPT-ko] itwiki "혼합 정밀도 학습" (mixed precision training)
+ *   [FP8-TE] llm-wiki "FP8 혼합 정밀도 LLM 학습: Transformer Engine과 Delayed Scaling…"
+ *   [NVFP4]  gist.science "Pretraining Large Language Models with NVFP4"
+ *   [MPT-es] marovi.ai "Mixed Precision Training/es"
+ *
+ * Conventions for every entry point:
+ *   - Pointers prefixed d_ and all tensor pointers are DEVICE pointers on the
+ *     current device; structs passed as `const T*` without the prefix are HOST
+ *     pointers read during the call only.  The caller owns every buffer; the
+ *     library never allocates, frees or synchronises.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work is enqueued on it and runs asynchronously.
+ *   - Argument errors are detected on the host and returned before anything
+ *     is enqueued.  A failed launch returns MP_ECUDA.  Data conditions
+ *     (inf/NaN in the grads, non-finite NVFP4 input) are reported through
+ *     device words, never through the return code.
+ *   - Tensors are dense, row-major and 16-byte aligned.  Element counts may
+ *     be anything >= 0 unless stated.
+ *   - Calls that share a state struct, meta struct or workspace must be
+ *     ordered on one stream; calls with disjoint state may run concurrently.
+ */
+#ifndef MPNUM_H
+#define MPNUM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MP_API __attribute__((visibility("default")))
+#else
+#define MP_API
+#endif
+
+typedef int32_t mp_status;
+enum {
+  MP_OK = 0,
+  MP_EINVAL = -1,     /* null pointer, negative size, bad enum or hyperparameter */
+  MP_EALIGN = -2,     /* a tensor pointer is not 16-byte aligned */
+  MP_ESHAPE = -3,     /* cols % 16 != 0, or rows % 16 != 0 for 16x16 blocks */
+  MP_EWORKSPACE = -4, /* workspace missing or smaller than required */
+  MP_ECUDA = -5       /* a kernel launch failed */
+};
+
+typedef int32_t mp_dtype;
+enum { MP_F32 = 0, MP_F16 = 1, MP_BF16 = 2, MP_E4M3 = 3, MP_E5M2 = 4 };
+
+MP_API const char* mp_status_str(mp_status s);
+MP_API int32_t mp_version(void);
+/* Number of kernels this library has launched in this process (diagnostic). */
+MP_API uint64_t mp_launch_count(void);
+
+/* =========================================================================
+ * 1. Mixed-precision optimizer step
+ * ========================================================================= */
+
+/* One parameter tensor of the step.  master, exp_avg, exp_avg_sq: FP32, read
+ * and written.  grad: 16-bit (F16 or BF16), read, holding S * dL/dw.
+ * working: 16-bit copy of the master, written.  All numel elements long. */
+typedef struct {
+  float* master;
+  float* exp_avg;
+  float* exp_avg_sq;
+  const void* grad;
+  void* working;
+  int64_t numel;
+} mp_param;
+
+/* AdamW hyperparameters ([MPT-ko] "FP16 학습 루프": AdamW, lr 1e-3). */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} mp_adamw_hparams;
+
+/* Device-resident state of the loss scaler and the step counter, 88 bytes.
+ * Copying the struct checkpoints it.  Initialise it with
+ * mp_scaler_state_init on the host and copy it to the device. */
+typedef struct {
+  float scale;            /* loss scale S in force for the next step */
+  int32_t growth_tracker; /* consecutive clean steps since the last change */
+  int32_t found_inf;      /* 1 if the most recent step saw an inf/NaN grad */
+  int32_t reserved0;
+  int64_t step;           /* applied (not skipped) optimizer steps */
+  double beta1_pow;       /* beta1^step */
+  double beta2_pow;       /* beta2^step */
+  int64_t skipped;        /* steps skipped because of inf/NaN */
+  /* library-internal: zero after mp_scaler_state_init, left zero between calls */
+  uint32_t internal_found;
+  uint32_t internal_ticket;
+  float internal_scalars[8];
+} mp_scaler_state;
+
+/* Loss-scale schedule ([MPT-ko] "손실 스케일링": GradScaler defaults 65536,
+ * growth 2, backoff 0.5, interval 2000). */
+typedef struct {
+  float growth_factor, backoff_factor;
+  int32_t growth_interval; /* >= 1 */
+  int32_t enabled;         /* 0: loss_scale_update leaves the state unchanged */
+} mp_scaler_cfg;
+
+/* Host helper: scale = init_scale, beta powers 1, everything else zero. */
+MP_API void mp_scaler_state_init(mp_scaler_state* host_state, float init_scale);
+
+/* mp_adamw_step — one fused mixed-precision optimizer step over n_params
+ * tensors ([MPT-ko] "FP32 마스터 가중치", "손실 스케일링", "FP16 학습 루프";
+ * [MPT-es] "La receta de precisión mixta", "Escalado dinámico de pérdida").
+ *
+ * Pass 1 reads every grad once and sets d_state->found_inf to 1 if any grad
+ * element is inf or NaN, else 0.  If it is set the step is skipped: no master,
+ * moment or working element is written and step / beta powers do not advance
+ * ([MPT-ko]: the update of that step is skipped).  Otherwise step += 1, the
+ * beta powers advance and every element is updated, in binary32, with
+ * scalars formed once per step in binary64 from the float hyperparameters:
+ *     g  = fp32(grad) * (1/S)                      unscale
+ *     w  = w * (1 - lr*wd)                         decoupled weight decay
+ *     m  = m*beta1 + g*(1-beta1)
+ *     v  = v*beta2 + (g*g)*(1-beta2)
+ *     w  = w - (lr/(1-beta1^t)) * (m / (sqrt(v)/sqrt(1-beta2^t) + eps))
+ *     working = round-to-nearest-even to the working dtype (NaN -> 0x7FFF)
+ * The host array `params` (n_params >= 0 entries) is read during the call
+ * only; its pointers are device pointers, 16-byte aligned.  grad_dtype and
+ * working_dtype are MP_F16 or MP_BF16.  The loss scale itself is not changed
+ * here: call loss_scale_update after the step.  Launches at most
+ * 2 * ceil(n_params / 512) kernels. */
+MP_API mp_status mp_adamw_step(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
+                               mp_dtype working_dtype, const mp_adamw_hparams* hp,
+                               mp_scaler_state* d_state, void* stream);
+
+/* The two passes of mp_adamw_step as separate calls, mirroring the unscale
+ * (inf check) and step calls of [MPT-ko] "FP16 학습 루프", so that work such
+ * as gradient-norm clipping can run between them.  mp_adamw_check is pass 1
+ * (sets found_inf, advances step / beta powers, forms the step scalars from
+ * hp); mp_adamw_apply is pass 2 and must follow it on the same stream with the
+ * same params and hp.  Each launches ceil(n_params / 512) kernels. */
+MP_API mp_status mp_adamw_check(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
+                                const mp_adamw_hparams* hp, mp_scaler_state* d_state, void* stream);
+MP_API mp_status mp_adamw_apply(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
+                                mp_dtype working_dtype, const mp_adamw_hparams* hp,
+                                mp_scaler_state* d_state, void* stream);
+
+/* loss_scale_update — the dynamic loss-scale schedule ([MPT-ko] "손실 스케일링";
+ * [MPT-es] "Escalado dinámico de pérdida"), from d_state->found_inf of the
+ * last step: on inf/NaN S *= backoff, tracker = 0, skipped += 1; otherwise
+ * tracker += 1 and when it reaches growth_interval S *= growth (kept only if
+ * finite) and tracker = 0.  One single-thread kernel. */
+MP_API mp_status loss_scale_update(mp_scaler_state* d_state, const mp_scaler_cfg* cfg,
+                                   void* stream);
+
+/* =========================================================================
+ * 2. FP8 delayed scaling
+ * ========================================================================= */
+
+/* Device-resident per-tensor FP8 metadata, 32 bytes. */
+typedef struct {
+  float scale;     /* scale used by the next cast */
+  float scale_inv; /* 1 / scale */
+  float amax;      /* amax of the most recent cast's input */
+  int32_t pos;     /* next history slot */
+  /* library-internal: zero after mp_fp8_meta_init, left zero between calls */
+  uint32_t internal_amax;
+  uint32_t internal_ticket;
+  uint32_t reserved[2];
+} mp_fp8_meta;
+
+/* Host helper: scale = scale_inv = 1, amax = 0, pos = 0, internals zero. */
+MP_API void mp_fp8_meta_init(mp_fp8_meta* host_meta);
+
+/* fp8_cast_delayed — one delayed-scaling cast ([FP8-TE] "Delayed Scaling 동작
+ * 원리", "E4M3 vs E5M2", "FP8이 어려운 이유"; [MPT-ko] "FP8 혼합 정밀도").
+ * Reads x once.  For each of the n elements of x (x_dtype MP_F32, MP_F16 or
+ * MP_BF16): y = saturate(round-to-nearest-even(fp32(x) * d_meta->scale)) in
+ * fp8_dtype (MP_E4M3: max 448; MP_E5M2: max 57344); magnitudes beyond the
+ * maximum, infinities included, become the signed maximum; NaN becomes 0x7F.
+ * In the same pass amax = max |x| (NaN if any element is NaN).  Then
+ * d_meta->amax = amax, d_history[p] = amax with p = pos mod history_len,
+ * pos = (p + 1) % history_len,
+ * and if H = max(d_history) is finite and > 0 the next scale is
+ * fp8_max / (margin * H) (kept only if finite and > 0), scale_inv = 1/scale.
+ * d_history: history_len FP32 entries (1..65536), zero-initialised by the
+ * caller, non-negative.  x and y 16-byte aligned. */
+MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
+                                  mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
+                                  int32_t history_len, float margin, void* stream);
+
+/* =========================================================================
+ * 3. NVFP4 quantisation and the random Hadamard transform
+ * ========================================================================= */
+
+/* Bytes of workspace nvfp4_quantize needs (zero-filled before first use;
+ * every completed call leaves it zero-filled again). */
+MP_API size_t nvfp4_workspace_size(void);
+
+/* nvfp4_quantize — two-level NVFP4 quantisation of a BF16 [rows, cols]
+ * tensor ([NVFP4] §2.1 "NVFP4 포맷의 특징", §2.2 items 2-4).
+ *   x' = x, or with apply_rht the 16-point transform of rht16 applied to
+ *        every 16 contiguous elements of each row;
+ *   s_t = amax(|x'|) / (6 * 448)                  -> *d_tensor_scale (FP32)
+ *   per block (1x16 along a row, or 16x16 when block_2d):
+ *        sb = E4M3(round-to-nearest-even((bamax / 6) / s_t)), saturating
+ *        d  = value(sb) * s_t,  r = 1/d (0 if d == 0 or 1/d not finite)
+ *   per element: q = E2M1(x' * r), saturating at 6, sign kept on zero,
+ *        round to nearest even, or with `stochastic` rounded away from zero
+ *        iff floor(frac * 2^16) + r16 >= 2^16, where frac is the position of
+ *        |x' r| between its grid neighbours and r16 are the 16 bits of
+ *        Philox4x32-10 (key = seed, counter = (i/8, 0, 0)) word (i/2)%4,
+ *        half i%2, i the flat row-major element index;
+ *   dequant (optional, may be NULL) = BF16 RNE of value(q) * d.
+ * Outputs: codes [rows, cols/2] (element 2j in the low nibble of byte j),
+ * block_scales [rows, cols/16] (1x16) or [rows/16, cols/16] (16x16), E4M3
+ * bytes, row-major; d_nonfinite = 1 if amax is not finite, in which case
+ * s_t = amax and all codes, scales and dequant values are zero (also when
+ * s_t == 0).  Requires cols % 16 == 0, and rows % 16 == 0 when block_2d.
+ * Two passes over x (amax, then encode): two kernel launches. */
+MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, int32_t block_2d,
+                                int32_t stochastic, uint64_t seed, int32_t apply_rht,
+                                uint16_t rht_sign_mask, uint8_t* codes, uint8_t* block_scales,
+                                float* d_tensor_scale, int32_t* d_nonfinite, void* dequant_bf16,
+                                void* d_workspace, size_t workspace_bytes, void* stream);
+
+/* rht16 — the 16-point random Hadamard transform ([NVFP4] §2.2 item 2):
+ * for every 16 contiguous elements t of each row of BF16 x [rows, cols],
+ * y_t = 1/4 * H16 * diag(s) * x_t, H16 the Sylvester Hadamard matrix
+ * (H[i][j] = (-1)^popcount(i & j)), s_j = -1 iff bit j of sign_mask is set,
+ * evaluated in binary32 by the butterfly of span 1, 2, 4, 8.  y_dtype MP_F32
+ * or MP_BF16 (round to nearest even).  cols % 16 == 0. */
+MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t sign_mask, void* y,
+                       mp_dtype y_dtype, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MPNUM_H */

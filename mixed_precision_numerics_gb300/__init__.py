@@ -1,0 +1,292 @@
+"""GB300 mixed-precision hot path: Python binding of libmpnum.so.
+
+The functions below carry the C entry points' names and only marshal
+arguments (tensor data pointers, the current CUDA stream, host structs); every
+step of the computation runs in the library's CUDA kernels.  Importing this
+package fails loudly when ``libmpnum.so`` has not been built: there is no
+other implementation to fall back to.
+
+PyTorch supplies device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Sequence
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmpnum.so")
+
+MP_OK, MP_EINVAL, MP_EALIGN, MP_ESHAPE, MP_EWORKSPACE, MP_ECUDA = 0, -1, -2, -3, -4, -5
+MP_F32, MP_F16, MP_BF16, MP_E4M3, MP_E5M2 = 0, 1, 2, 3, 4
+
+
+class MpParam(ctypes.Structure):
+    _fields_ = [
+        ("master", ctypes.c_void_p),
+        ("exp_avg", ctypes.c_void_p),
+        ("exp_avg_sq", ctypes.c_void_p),
+        ("grad", ctypes.c_void_p),
+        ("working", ctypes.c_void_p),
+        ("numel", ctypes.c_int64),
+    ]
+
+
+class AdamwHparams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")]
+
+
+class ScalerState(ctypes.Structure):
+    _fields_ = [
+        ("scale", ctypes.c_float),
+        ("growth_tracker", ctypes.c_int32),
+        ("found_inf", ctypes.c_int32),
+        ("reserved0", ctypes.c_int32),
+        ("step", ctypes.c_int64),
+        ("beta1_pow", ctypes.c_double),
+        ("beta2_pow", ctypes.c_double),
+        ("skipped", ctypes.c_int64),
+        ("internal_found", ctypes.c_uint32),
+        ("internal_ticket", ctypes.c_uint32),
+        ("internal_scalars", ctypes.c_float * 8),
+    ]
+
+
+class ScalerCfg(ctypes.Structure):
+    _fields_ = [
+        ("growth_factor", ctypes.c_float),
+        ("backoff_factor", ctypes.c_float),
+        ("growth_interval", ctypes.c_int32),
+        ("enabled", ctypes.c_int32),
+    ]
+
+
+class Fp8Meta(ctypes.Structure):
+    _fields_ = [
+        ("scale", ctypes.c_float),
+        ("scale_inv", ctypes.c_float),
+        ("amax", ctypes.c_float),
+        ("pos", ctypes.c_int32),
+        ("internal_amax", ctypes.c_uint32),
+        ("internal_ticket", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32 * 2),
+    ]
+
+
+assert ctypes.sizeof(ScalerState) == 88 and ctypes.sizeof(Fp8Meta) == 32 and ctypes.sizeof(MpParam) == 48
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(nvcc, sm_103a). There is no fallback implementation."
+        )
+    L = ctypes.CDLL(LIB_PATH)
+    P, I32, I64, U16, U64, F, S = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint16,
+                                   ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t)
+    sig = {
+        "mp_status_str": (ctypes.c_char_p, [I32]),
+        "mp_version": (I32, []),
+        "mp_launch_count": (U64, []),
+        "mp_scaler_state_init": (None, [P, F]),
+        "mp_fp8_meta_init": (None, [P]),
+        "mp_adamw_step": (I32, [P, I32, I32, I32, P, P, P]),
+        "mp_adamw_check": (I32, [P, I32, I32, P, P, P]),
+        "mp_adamw_apply": (I32, [P, I32, I32, I32, P, P, P]),
+        "loss_scale_update": (I32, [P, P, P]),
+        "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, P]),
+        "nvfp4_workspace_size": (S, []),
+        "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
+        "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+class MpError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {lib.mp_status_str(status).decode()} (status {status})")
+        self.status = status
+
+
+def _check(fn: str, status: int) -> None:
+    if status != MP_OK:
+        raise MpError(fn, status)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    import torch
+
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    return {torch.float32: MP_F32, torch.float16: MP_F16, torch.bfloat16: MP_BF16}[t.dtype]
+
+
+def mp_status_str(status: int) -> str:
+    return lib.mp_status_str(status).decode()
+
+
+def mp_launch_count() -> int:
+    return int(lib.mp_launch_count())
+
+
+def nvfp4_workspace_size() -> int:
+    return int(lib.nvfp4_workspace_size())
+
+
+# ---- state helpers ------------------------------------------------------------------
+
+
+def scaler_state_bytes(init_scale: float = 65536.0) -> bytes:
+    st = ScalerState()
+    lib.mp_scaler_state_init(ctypes.byref(st), float(init_scale))
+    return bytes(st)
+
+
+def fp8_meta_bytes() -> bytes:
+    m = Fp8Meta()
+    lib.mp_fp8_meta_init(ctypes.byref(m))
+    return bytes(m)
+
+
+def new_scaler_state(init_scale: float = 65536.0, device="cuda"):
+    """Device buffer (uint8[88]) holding an initialised mp_scaler_state."""
+    import torch
+
+    return torch.frombuffer(bytearray(scaler_state_bytes(init_scale)), dtype=torch.uint8).to(device)
+
+
+def new_fp8_meta(device="cuda"):
+    import torch
+
+    return torch.frombuffer(bytearray(fp8_meta_bytes()), dtype=torch.uint8).to(device)
+
+
+def new_nvfp4_workspace(device="cuda"):
+    import torch
+
+    return torch.zeros(nvfp4_workspace_size(), dtype=torch.uint8, device=device)
+
+
+def read_scaler_state(t) -> ScalerState:
+    return ScalerState.from_buffer_copy(t.cpu().numpy().tobytes())
+
+
+def read_fp8_meta(t) -> Fp8Meta:
+    return Fp8Meta.from_buffer_copy(t.cpu().numpy().tobytes())
+
+
+# ---- entry points ---------------------------------------------------------------------
+
+
+@dataclass
+class Param:
+    """One parameter tensor of the step (torch CUDA tensors, contiguous)."""
+
+    master: object
+    exp_avg: object
+    exp_avg_sq: object
+    grad: object
+    working: object
+
+
+def make_param_array(params: Sequence[Param]):
+    arr = (MpParam * max(1, len(params)))()
+    for i, p in enumerate(params):
+        arr[i] = MpParam(_ptr(p.master), _ptr(p.exp_avg), _ptr(p.exp_avg_sq), _ptr(p.grad), _ptr(p.working),
+                         p.master.numel())
+    return arr
+
+
+def mp_adamw_step(params, hp: AdamwHparams, state, grad_dtype: int | None = None,
+                  working_dtype: int | None = None, stream=None) -> None:
+    """params: a sequence of Param, or a prebuilt ctypes MpParam array (then give dtypes)."""
+    arr, n, g, w = _marshal(params, grad_dtype, working_dtype)
+    _check("mp_adamw_step", lib.mp_adamw_step(arr, n, g, w, ctypes.byref(hp), _ptr(state), _stream(stream)))
+
+
+def _marshal(params, grad_dtype, working_dtype):
+    if isinstance(params, ctypes.Array):
+        assert grad_dtype is not None and working_dtype is not None
+        return params, len(params), grad_dtype, working_dtype
+    n = len(params)
+    arr = make_param_array(params)
+    if grad_dtype is None:
+        grad_dtype = _dtype_code(params[0].grad) if n else MP_F16
+    if working_dtype is None:
+        working_dtype = _dtype_code(params[0].working) if n else MP_F16
+    return arr, n, grad_dtype, working_dtype
+
+
+def mp_adamw_check(params, hp: AdamwHparams, state, grad_dtype: int | None = None, stream=None) -> None:
+    arr, n, g, _ = _marshal(params, grad_dtype, MP_F16 if grad_dtype is not None else None)
+    _check("mp_adamw_check", lib.mp_adamw_check(arr, n, g, ctypes.byref(hp), _ptr(state), _stream(stream)))
+
+
+def mp_adamw_apply(params, hp: AdamwHparams, state, grad_dtype: int | None = None,
+                   working_dtype: int | None = None, stream=None) -> None:
+    arr, n, g, w = _marshal(params, grad_dtype, working_dtype)
+    _check("mp_adamw_apply", lib.mp_adamw_apply(arr, n, g, w, ctypes.byref(hp), _ptr(state), _stream(stream)))
+
+
+def loss_scale_update(state, cfg: ScalerCfg, stream=None) -> None:
+    _check("loss_scale_update", lib.loss_scale_update(_ptr(state), ctypes.byref(cfg), _stream(stream)))
+
+
+def fp8_cast_delayed(x, y, fp8_dtype: int, meta, history, margin: float = 1.0, stream=None,
+                     n: int | None = None) -> None:
+    """y: uint8 (or float8) tensor with x.numel() elements; history: float32 device tensor."""
+    _check("fp8_cast_delayed",
+           lib.fp8_cast_delayed(_ptr(x), _dtype_code(x), x.numel() if n is None else n, _ptr(y), fp8_dtype,
+                                _ptr(meta), _ptr(history), history.numel(), float(margin), _stream(stream)))
+
+
+def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *, block_2d: bool = False,
+                   stochastic: bool = False, seed: int = 0, apply_rht: bool = False, sign_mask: int = 0,
+                   dequant=None, rows: int | None = None, cols: int | None = None, stream=None) -> None:
+    if rows is None:
+        rows, cols = x.shape
+    _check("nvfp4_quantize",
+           lib.nvfp4_quantize(_ptr(x), rows, cols, int(block_2d), int(stochastic), seed & (2**64 - 1),
+                              int(apply_rht), sign_mask & 0xFFFF, _ptr(codes), _ptr(block_scales),
+                              _ptr(tensor_scale), _ptr(nonfinite), _ptr(dequant), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rht16(x, y, sign_mask: int, stream=None) -> None:
+    rows, cols = x.shape
+    _check("rht16", lib.rht16(_ptr(x), rows, cols, sign_mask & 0xFFFF, _ptr(y), _dtype_code(y), _stream(stream)))
+
+
+__all__ = [
+    "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
+    "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
+    "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "loss_scale_update", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
+    "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
+    "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",
+    "make_param_array",
+]

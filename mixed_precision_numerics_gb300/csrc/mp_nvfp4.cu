@@ -1,0 +1,403 @@
+// mp_nvfp4.cu — NVFP4 quantisation and the 16-point random Hadamard transform.
+//
+// [NVFP4] gist.science "Pretraining Large Language Models with NVFP4":
+//   §2.1 "NVFP4 포맷의 특징": 16-element blocks, E4M3 block scale, FP32 tensor
+//        scale (two-level scaling), FP4 (E2M1) elements;
+//   §2.2 item 2: 16x16 random Hadamard transform of weight-gradient inputs;
+//   §2.2 item 3: 16x16 2D block scaling for weights, 1x16 for the rest;
+//   §2.2 item 4: stochastic rounding for gradients.
+//
+// Two passes, because the tensor scale needs the amax of the whole tensor
+// before any element can be encoded:
+//   k_nvfp4_amax    reads x (2 B/elem), applies the transform when asked,
+//                   folds max |x'| with one atomicMax per CTA; the last CTA
+//                   (ticket, no waiting) writes s_t = amax / 2688.
+//   k_nvfp4_1x16 /  read x again, recompute x', form block scales, encode,
+//   k_nvfp4_2d      pack two codes per byte (0.5 B/elem) and one scale byte
+//                   per block.
+// The transform is evaluated on CUDA cores by the butterfly in binary32 so
+// that its additions happen in the documented order.
+#include "mp_device.cuh"
+#include "mp_internal.h"
+
+namespace mp {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kTensorDiv = 2688.0f;  // 6 (largest E2M1) * 448 (largest E4M3)
+
+struct Ws {
+  uint32_t amax_bits;
+  uint32_t ticket;
+};
+
+// Load one 16-element tile of BF16 and produce x' in binary32.
+template <bool RHT>
+__device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw, float (&v)[16]) {
+  uint4 a = ld_plain(p), b = ld_plain(p + 8);
+  if (RHT) apply_signs(a, b, sw);
+  unpack_bf16x16(a, b, v);
+  if (RHT) {
+    fwht16(v);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+  }
+}
+
+template <bool RHT>
+__global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restrict__ x, int64_t ntiles,
+                                                         uint32_t mask, Ws* ws, float* tensor_scale,
+                                                         int32_t* nonfinite) {
+  __shared__ uint32_t red[32];
+  __shared__ int is_last;
+  const SignWords sw = sign_words(mask);
+  float acc = 0.0f;
+  constexpr int U = 2;
+  const int64_t step = (int64_t)gridDim.x * kThreads * U;
+  for (int64_t t0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; t0 < ntiles; t0 += step) {
+    uint4 a[U], b[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t t = t0 + (int64_t)u * kThreads;
+      if (t < ntiles) {
+        a[u] = ld_plain(x + t * 16);
+        b[u] = ld_plain(x + t * 16 + 8);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t t = t0 + (int64_t)u * kThreads;
+      if (t >= ntiles) continue;
+      if (RHT) apply_signs(a[u], b[u], sw);
+      float v[16];
+      unpack_bf16x16(a[u], b[u], v);
+      if (RHT) fwht16(v);  // the 1/4 is applied once to the maximum below
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc = max_abs_nan(acc, v[j]);
+    }
+  }
+  const uint32_t cta = block_max_u32(amax_bits(acc), red);
+  if (threadIdx.x == 0) {
+    atomicMax(&ws->amax_bits, cta);
+    __threadfence();
+    is_last = atomicAdd(&ws->ticket, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!is_last || threadIdx.x != 0) return;
+  __threadfence();
+  const uint32_t ab = atomicExch(&ws->amax_bits, 0u);
+  ws->ticket = 0;
+  // Rounding is monotonic, so max(round(|v| / 4)) == round(max|v| / 4).
+  float amax = __uint_as_float(ab);
+  if (RHT) amax = __fmul_rn(amax, 0.25f);
+  if (amax != amax) {
+    *tensor_scale = __uint_as_float(0x7FC00000u);
+    *nonfinite = 1;
+  } else if (isinf(amax)) {
+    *tensor_scale = amax;
+    *nonfinite = 1;
+  } else {
+    *tensor_scale = __fdiv_rn(amax, kTensorDiv);
+    *nonfinite = 0;
+  }
+}
+
+struct BlockScale {
+  uint32_t code;
+  float d, r;
+};
+
+// sb = E4M3(RNE((bamax / 6) / s_t)) saturating; d = value(sb) * s_t; r = 1/d.
+__device__ __forceinline__ BlockScale block_scale(float bamax, float s_t) {
+  BlockScale bs;
+  const float q = fminf(__fdiv_rn(__fdiv_rn(bamax, 6.0f), s_t), 448.0f);
+  bs.code = cvt_e4m3x2(q, 0.0f) & 0xFFu;
+  bs.d = __fmul_rn(e4m3_pos_to_f32(bs.code), s_t);
+  bs.r = 0.0f;
+  if (bs.d != 0.0f) {
+    const float inv = __fdiv_rn(1.0f, bs.d);
+    if (isfinite(inv)) bs.r = inv;
+  }
+  return bs;
+}
+
+// Stochastic E2M1 code of y with 16 random bits: round away from zero iff
+// floor(frac * 2^16) + r16 >= 2^16.  For |y| >= 1 the 22 fraction bits below
+// the kept mantissa bit of |y| are exactly frac * 2^22; for |y| < 1 the same
+// holds for the bits of 1 + |y| truncated to binary32.  Adding r16 at bit 6
+// carries into bit 22 exactly when the rule rounds up.
+__device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r16) {
+  const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
+  const float a = fminf(fabsf(y), 6.0f);
+  const bool sub = a < 1.0f;
+  const float b = sub ? __fadd_rz(a, 1.0f) : a;
+  const uint32_t adj = sub ? (254u << 22) : (252u << 22);
+  return (((__float_as_uint(b) + (r16 << 6)) - adj) >> 22) | sign;
+}
+
+// Encode 16 values of x' with block reciprocal r; returns 8 packed bytes.
+// `flat` is the flat index of the first element (a multiple of 16).
+template <bool SR>
+__device__ __forceinline__ uint2 encode16(const float (&v)[16], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
+  uint32_t lo = 0, hi = 0;
+  if (SR) {
+    const uint64_t g = flat >> 3;
+    const u32x4 R0 = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
+    const uint64_t g1 = g + 1;
+    const u32x4 R1 = philox4x32_10((uint32_t)g1, (uint32_t)(g1 >> 32), 0u, 0u, k0, k1);
+    const uint32_t words[8] = {R0.x, R0.y, R0.z, R0.w, R1.x, R1.y, R1.z, R1.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t w = words[j >> 1];
+      const uint32_t r16 = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+      const uint32_t c = sr_e2m1(__fmul_rn(v[j], r), r16);
+      if (j < 8) lo |= c << (4 * j);
+      else hi |= c << (4 * (j - 8));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t c = cvt_e2m1x2(__fmul_rn(v[2 * k], r), __fmul_rn(v[2 * k + 1], r));
+      if (k < 4) lo |= c << (8 * k);
+      else hi |= c << (8 * (k - 4));
+    }
+  }
+  return make_uint2(lo, hi);
+}
+
+// BF16 RNE of value(code) * d for the 16 codes in (lo, hi).
+__device__ __forceinline__ void dequant16(uint2 q, float d, uint16_t* out) {
+  uint32_t w[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const uint32_t byte = ((k < 4 ? q.x : q.y) >> (8 * (k & 3))) & 0xFFu;
+    w[k] = pack_bf16x2(__fmul_rn(e2m1_to_f32(byte & 0xFu), d), __fmul_rn(e2m1_to_f32(byte >> 4), d));
+  }
+  st_cs(out, make_uint4(w[0], w[1], w[2], w[3]));
+  st_cs(out + 8, make_uint4(w[4], w[5], w[6], w[7]));
+}
+
+template <bool RHT, bool SR, bool DEQ>
+__global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restrict__ x, int64_t nblocks,
+                                                         uint32_t mask, uint64_t seed,
+                                                         const float* __restrict__ tensor_scale,
+                                                         const int32_t* __restrict__ nonfinite,
+                                                         uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                         uint16_t* __restrict__ deq) {
+  const float s_t = *tensor_scale;
+  const bool zero = (*nonfinite != 0) || s_t == 0.0f;
+  const SignWords sw = sign_words(mask);
+  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t blk = (int64_t)blockIdx.x * kThreads + threadIdx.x; blk < nblocks; blk += stride) {
+    if (zero) {
+      *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(0u, 0u);
+      scales[blk] = 0;
+      if (DEQ) {
+        st_cs(deq + blk * 16, make_uint4(0u, 0u, 0u, 0u));
+        st_cs(deq + blk * 16 + 8, make_uint4(0u, 0u, 0u, 0u));
+      }
+      continue;
+    }
+    float v[16];
+    load_tile<RHT>(x + blk * 16, sw, v);
+    float bamax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) bamax = fmaxf(bamax, fabsf(v[j]));
+    const BlockScale bs = block_scale(bamax, s_t);
+    const uint2 q = encode16<SR>(v, bs.r, (uint64_t)blk * 16, k0, k1);
+    __stcs(reinterpret_cast<uint2*>(codes + blk * 8), q);
+    scales[blk] = (uint8_t)bs.code;
+    if (DEQ) dequant16(q, bs.d, deq + blk * 16);
+  }
+}
+
+// 16x16 blocks: a CTA covers 16 rows x 256 columns (16 tiles).  Thread t
+// handles row t/16 and the 16-column segment t%16; the tile amax is combined
+// across the two rows a warp holds by shuffle and across warps in shared
+// memory.
+template <bool RHT, bool SR, bool DEQ>
+__global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
+                                                       uint32_t mask, uint64_t seed,
+                                                       const float* __restrict__ tensor_scale,
+                                                       const int32_t* __restrict__ nonfinite,
+                                                       uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
+                                                       uint16_t* __restrict__ deq) {
+  __shared__ float tile_max[8][16];
+  const float s_t = *tensor_scale;
+  const bool zero = (*nonfinite != 0) || s_t == 0.0f;
+  const SignWords sw = sign_words(mask);
+  const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+  const int r = threadIdx.x >> 4, seg = threadIdx.x & 15, warp = threadIdx.x >> 5;
+  const int64_t ncc = (cols + 255) / 256;
+  const int64_t nitems = (rows / 16) * ncc;
+  const int64_t nb = cols / 16;
+  for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const int64_t tr = item / ncc, cc = item % ncc;
+    const int64_t row = tr * 16 + r;
+    const int64_t col = cc * 256 + seg * 16;
+    const bool active = col < cols;
+    const int64_t flat = row * cols + col;
+    float v[16];
+    float m = 0.0f;
+    if (active && !zero) {
+      load_tile<RHT>(x + flat, sw, v);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    if ((threadIdx.x & 31) < 16) tile_max[warp][seg] = m;
+    __syncthreads();
+    float bamax = tile_max[0][seg];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) bamax = fmaxf(bamax, tile_max[w][seg]);
+    __syncthreads();  // tile_max is rewritten by the next item
+    if (!active) continue;
+    if (zero) {
+      *reinterpret_cast<uint2*>(codes + flat / 2) = make_uint2(0u, 0u);
+      if (r == 0) scales[tr * nb + col / 16] = 0;
+      if (DEQ) {
+        st_cs(deq + flat, make_uint4(0u, 0u, 0u, 0u));
+        st_cs(deq + flat + 8, make_uint4(0u, 0u, 0u, 0u));
+      }
+      continue;
+    }
+    const BlockScale bs = block_scale(bamax, s_t);
+    const uint2 q = encode16<SR>(v, bs.r, (uint64_t)flat, k0, k1);
+    __stcs(reinterpret_cast<uint2*>(codes + flat / 2), q);
+    if (r == 0) scales[tr * nb + col / 16] = (uint8_t)bs.code;
+    if (DEQ) dequant16(q, bs.d, deq + flat);
+  }
+}
+
+template <bool F32OUT>
+__global__ __launch_bounds__(kThreads) void k_rht16(const uint16_t* __restrict__ x, int64_t ntiles, uint32_t mask,
+                                                    void* __restrict__ y) {
+  const SignWords sw = sign_words(mask);
+  const int64_t stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < ntiles; t += stride) {
+    float v[16];
+    load_tile<true>(x + t * 16, sw, v);
+    if (F32OUT) {
+      float* o = static_cast<float*>(y) + t * 16;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) st_cs_f4(o + 4 * k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+    } else {
+      uint16_t* o = static_cast<uint16_t*>(y) + t * 16;
+      uint32_t w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+      st_cs(o, make_uint4(w[0], w[1], w[2], w[3]));
+      st_cs(o + 8, make_uint4(w[4], w[5], w[6], w[7]));
+    }
+  }
+}
+
+template <typename K>
+int occ_of(K kernel) {
+  int o = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kThreads, 0) != cudaSuccess || o < 1) o = 1;
+  return o;
+}
+
+template <bool RHT>
+void launch_amax(const uint16_t* x, int64_t ntiles, uint32_t mask, Ws* ws, float* ts, int32_t* nf, cudaStream_t s) {
+  static const int occ = occ_of(k_nvfp4_amax<RHT>);
+  const int64_t ctas = (ntiles + 2 * kThreads - 1) / (2 * kThreads);
+  k_nvfp4_amax<RHT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, mask, ws, ts, nf);
+}
+
+template <bool RHT, bool SR, bool DEQ>
+void launch_encode(bool block_2d, const uint16_t* x, int64_t rows, int64_t cols, uint32_t mask, uint64_t seed,
+                   const float* ts, const int32_t* nf, uint8_t* codes, uint8_t* scales, uint16_t* deq,
+                   cudaStream_t s) {
+  if (block_2d) {
+    static const int occ = occ_of(k_nvfp4_2d<RHT, SR, DEQ>);
+    const int64_t items = (rows / 16) * ((cols + 255) / 256);
+    k_nvfp4_2d<RHT, SR, DEQ><<<grid_for(items, occ), kThreads, 0, s>>>(x, rows, cols, mask, seed, ts, nf, codes,
+                                                                        scales, deq);
+  } else {
+    static const int occ = occ_of(k_nvfp4_1x16<RHT, SR, DEQ>);
+    const int64_t nblocks = rows * (cols / 16);
+    const int64_t ctas = (nblocks + kThreads - 1) / kThreads;
+    k_nvfp4_1x16<RHT, SR, DEQ><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, nblocks, mask, seed, ts, nf, codes,
+                                                                         scales, deq);
+  }
+}
+
+template <bool RHT, bool SR>
+void dispatch_deq(bool deq, bool block_2d, const uint16_t* x, int64_t rows, int64_t cols, uint32_t mask,
+                  uint64_t seed, const float* ts, const int32_t* nf, uint8_t* codes, uint8_t* scales,
+                  uint16_t* dq, cudaStream_t s) {
+  if (deq) launch_encode<RHT, SR, true>(block_2d, x, rows, cols, mask, seed, ts, nf, codes, scales, dq, s);
+  else launch_encode<RHT, SR, false>(block_2d, x, rows, cols, mask, seed, ts, nf, codes, scales, dq, s);
+}
+
+}  // namespace
+}  // namespace mp
+
+extern "C" {
+
+MP_API size_t nvfp4_workspace_size(void) { return 256; }
+
+MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, int32_t block_2d,
+                                int32_t stochastic, uint64_t seed, int32_t apply_rht, uint16_t rht_sign_mask,
+                                uint8_t* codes, uint8_t* block_scales, float* d_tensor_scale,
+                                int32_t* d_nonfinite, void* dequant_bf16, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  using namespace mp;
+  if (rows < 0 || cols < 0 || !d_tensor_scale || !d_nonfinite) return MP_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x_bf16 || !codes || !block_scales)) return MP_EINVAL;
+  if (cols % 16 != 0 || (block_2d && rows % 16 != 0)) return MP_ESHAPE;
+  if (!d_workspace || workspace_bytes < nvfp4_workspace_size()) return MP_EWORKSPACE;
+  if ((n > 0 && (!aligned16(x_bf16) || !aligned16(codes))) || (dequant_bf16 && !aligned16(dequant_bf16)) ||
+      (reinterpret_cast<uintptr_t>(d_tensor_scale) & 3u) || (reinterpret_cast<uintptr_t>(d_nonfinite) & 3u) ||
+      (reinterpret_cast<uintptr_t>(d_workspace) & 7u))
+    return MP_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  Ws* ws = static_cast<Ws*>(d_workspace);
+  uint16_t* dq = static_cast<uint16_t*>(dequant_bf16);
+  const uint32_t mask = rht_sign_mask;
+  const bool b2 = block_2d != 0, deq = dq != nullptr;
+  if (apply_rht) launch_amax<true>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, s);
+  else launch_amax<false>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, s);
+  if (apply_rht && stochastic)
+    dispatch_deq<true, true>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
+  else if (apply_rht)
+    dispatch_deq<true, false>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
+  else if (stochastic)
+    dispatch_deq<false, true>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
+  else
+    dispatch_deq<false, false>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
+  note_launches(2);
+  return launch_status();
+}
+
+MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t sign_mask, void* y,
+                       mp_dtype y_dtype, void* stream) {
+  using namespace mp;
+  if (rows < 0 || cols < 0) return MP_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x_bf16 || !y)) return MP_EINVAL;
+  if (y_dtype != MP_F32 && y_dtype != MP_BF16) return MP_EINVAL;
+  if (cols % 16 != 0) return MP_ESHAPE;
+  if (n > 0 && (!aligned16(x_bf16) || !aligned16(y))) return MP_EALIGN;
+  if (n == 0) return MP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int64_t ntiles = n / 16;
+  const int64_t ctas = (ntiles + kThreads - 1) / kThreads;
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  if (y_dtype == MP_F32) {
+    static const int occ = occ_of(k_rht16<true>);
+    k_rht16<true><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, sign_mask, y);
+  } else {
+    static const int occ = occ_of(k_rht16<false>);
+    k_rht16<false><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, sign_mask, y);
+  }
+  note_launches(1);
+  return launch_status();
+}
+
+}  // extern "C"

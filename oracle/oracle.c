@@ -381,8 +381,10 @@ void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt
 void orc_fp8_history_update(orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
                             float amax, int fmt) {
   meta->amax = amax;
-  history[meta->pos] = amax;
-  meta->pos = (meta->pos + 1) % hist_len;
+  /* reading R9b: the ring slot is pos taken modulo the ring length */
+  int32_t pos = ((meta->pos % hist_len) + hist_len) % hist_len;
+  history[pos] = amax;
+  meta->pos = (pos + 1) % hist_len;
   float hmax = 0.0f;
   for (int32_t i = 0; i < hist_len; ++i) {
     if (isnan(history[i])) { hmax = history[i]; break; }

@@ -91,6 +91,8 @@ def host():
         L.synth_logf_host.argtypes = [ctypes.c_float]
         L.synth_cos2pi_host.restype = ctypes.c_float
         L.synth_cos2pi_host.argtypes = [ctypes.c_float]
+        L.synth_hash_host.restype = ctypes.c_uint64
+        L.synth_hash_host.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
         _host = L
     return _host
 
@@ -107,6 +109,10 @@ def dev():
                                         ctypes.c_void_p, ctypes.c_void_p]
         _dev = L
     return _dev
+
+
+def hash64(seed: int, stream: int, index: int) -> int:
+    return int(host().synth_hash_host(seed, stream, index))
 
 
 def _threads() -> int:

@@ -82,3 +82,6 @@ float synth_normal_at(uint64_t seed, uint64_t stream, uint64_t index) {
 float synth_logf_host(float u) { return synth_logf(u); }
 float synth_cos2pi_host(float v) { return synth_cos2pi(v); }
 uint16_t synth_trunc_f16_host(float x) { return synth_trunc_f16(x); }
+uint64_t synth_hash_host(uint64_t seed, uint64_t stream, uint64_t index) {
+  return synth_hash(seed, stream, index);
+}

@@ -1,0 +1,242 @@
+"""GPU parity: mp_adamw_step + loss_scale_update (C ABI) against the oracle.
+
+The FP32 master, moments and step state must agree within 4 ulp (the order
+of operations is fixed on both sides, so 0 is expected and reported); the
+16-bit working copy and every scaler field bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+import synth.workloads as W
+from tests.conftest import golden
+from tests.gpu_util import to_dev, to_host, ulp_diff
+
+pytestmark = pytest.mark.gpu
+
+M = pytest.importorskip("mixed_precision_numerics_gb300")
+TD = {O.F16: torch.float16, O.BF16: torch.bfloat16}
+MPD = {O.F16: M.MP_F16, O.BF16: M.MP_BF16}
+MAX_ULP = 4
+
+
+@pytest.fixture(autouse=True)
+def _gpu(cuda_ok):
+    yield
+
+
+def hp_of(c):
+    return M.AdamwHparams(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay), O.AdamwHp(c.lr, c.beta1, c.beta2, c.eps,
+                                                                                     c.weight_decay)
+
+
+def assert_state_equal(g, o):
+    assert np.float32(g.scale) == np.float32(o.scale)
+    assert g.growth_tracker == o.growth_tracker and g.found_inf == o.found_inf
+    assert g.step == o.step and g.skipped == o.skipped
+    assert g.beta1_pow == o.beta1_pow and g.beta2_pow == o.beta2_pow
+    assert g.internal_found == 0 and g.internal_ticket == 0
+
+
+class Tensors:
+    def __init__(self, w0, g_fmt, w_fmt):
+        n = w0.size
+        self.w = to_dev(w0)
+        self.m = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.v = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.g = torch.zeros(n, dtype=TD[g_fmt], device="cuda")
+        self.w16 = torch.zeros(n, dtype=TD[w_fmt], device="cuda")
+        self.ow, self.om, self.ov = w0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        self.ow16 = np.zeros(n, np.uint16)
+
+    def param(self):
+        return M.Param(self.w, self.m, self.v, self.g, self.w16)
+
+    def oracle_tuple(self, g_host):
+        return (self.ow, self.om, self.ov, g_host, self.ow16)
+
+    def compare(self, what=""):
+        for gt, ot, name in ((self.w, self.ow, "w"), (self.m, self.om, "m"), (self.v, self.ov, "v")):
+            d = ulp_diff(gt.cpu().numpy(), ot)
+            assert d.max(initial=0) <= MAX_ULP, f"{what} {name}: max ulp {d.max()}"
+            assert d.max(initial=0) == 0, f"{what} {name}: max ulp {d.max()} (within tolerance but not exact)"
+        np.testing.assert_array_equal(to_host(self.w16, np.uint16), self.ow16, err_msg=f"{what} working copy")
+
+
+def test_tiny_step_twelve_steps():
+    c = W.TINY
+    t = golden("scaler_trajectory_tiny.json")
+    ghp, ohp = hp_of(c)
+    cfg = M.ScalerCfg(c.growth, c.backoff, c.interval, 1)
+    ocfg = O.ScalerCfg(c.growth, c.backoff, c.interval, 1)
+    w0 = synth.fill(c.master_recipe(), synth.F32, c.n)
+    T = Tensors(w0, O.F16, O.F16)
+    st = M.new_scaler_state(c.init_scale)
+    ost = O.new_scaler_state(c.init_scale)
+    for k in range(1, c.steps + 1):
+        S = t["scale_used"][k - 1]
+        assert M.read_scaler_state(st).scale == S
+        g = synth.fill(c.grad_recipe(k, S), synth.F16, c.n)
+        inj = c.injection(k)
+        if inj:
+            g[inj[0]] = inj[1]
+        T.g.copy_(to_dev(g, torch.float16))
+        M.mp_adamw_step([T.param()], ghp, st)
+        M.loss_scale_update(st, cfg)
+        O.adamw_step(ohp, ost, [T.oracle_tuple(g)], O.F16, O.F16)
+        O.loss_scale_update(ost, ocfg)
+        torch.cuda.synchronize()
+        gs = M.read_scaler_state(st)
+        assert gs.found_inf == t["found_inf"][k - 1]
+        assert gs.growth_tracker == t["tracker_after"][k - 1]
+        assert_state_equal(gs, ost)
+        T.compare(f"step {k}")
+    gs = M.read_scaler_state(st)
+    assert gs.scale == t["final_scale"] and gs.step == t["applied_steps"] and gs.skipped == t["skipped_steps"]
+
+
+@pytest.mark.parametrize("g_fmt,w_fmt", [(O.F16, O.F16), (O.F16, O.BF16), (O.BF16, O.BF16), (O.BF16, O.F16)])
+def test_ragged_multi_tensor(g_fmt, w_fmt):
+    sizes = [1, 7, 8, 9, 15, 4095, 4096, 4097, 8191, 100_003, 0, 3]
+    ghp, ohp = M.AdamwHparams(3e-3, 0.8, 0.99, 1e-6, 0.1), O.AdamwHp(3e-3, 0.8, 0.99, 1e-6, 0.1)
+    cfg, ocfg = M.ScalerCfg(2.0, 0.5, 2, 1), O.ScalerCfg(2.0, 0.5, 2, 1)
+    S0 = 1024.0 if g_fmt == O.F16 else 1.0
+    Ts = [Tensors(synth.fill(synth.recipe(20, i, 0.5), synth.F32, n), g_fmt, w_fmt) for i, n in enumerate(sizes)]
+    st, ost = M.new_scaler_state(S0), O.new_scaler_state(S0)
+    for k in range(1, 5):
+        S = float(ost.scale)
+        hosts = []
+        for i, (T, n) in enumerate(zip(Ts, sizes)):
+            g = synth.fill(synth.recipe(21, 100 * k + i, float(np.float32(0.01 * S))), synth.F16 if g_fmt == O.F16
+                           else synth.BF16, n)
+            if k == 2 and i == 5:
+                g[17] = 0x7C00 if g_fmt == O.F16 else 0xFF80  # +inf / -inf
+            hosts.append(g)
+            if n:
+                T.g.copy_(to_dev(g, TD[g_fmt]))
+        M.mp_adamw_step([T.param() for T in Ts], ghp, st)
+        M.loss_scale_update(st, cfg)
+        O.adamw_step(ohp, ost, [T.oracle_tuple(g) for T, g in zip(Ts, hosts)], g_fmt, w_fmt)
+        O.loss_scale_update(ost, ocfg)
+        torch.cuda.synchronize()
+        assert_state_equal(M.read_scaler_state(st), ost)
+        for i, T in enumerate(Ts):
+            T.compare(f"step {k} tensor {i}")
+    assert ost.skipped == 1
+
+
+def test_more_tensors_than_one_launch_table():
+    rng = np.random.default_rng(3)
+    sizes = rng.integers(1, 300, size=600).tolist()
+    ghp, ohp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.01), O.AdamwHp(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    Ts = [Tensors(synth.fill(synth.recipe(30, i, 0.02), synth.F32, n), O.BF16, O.BF16) for i, n in enumerate(sizes)]
+    st, ost = M.new_scaler_state(1.0), O.new_scaler_state(1.0)
+    for k in (1, 2):
+        hosts = []
+        for i, (T, n) in enumerate(zip(Ts, sizes)):
+            g = synth.fill(synth.recipe(31, 1000 * k + i, 1e-3), synth.BF16, n)
+            if k == 2 and i == 550:
+                g[0] = 0x7FC0  # NaN in the second launch group
+            hosts.append(g)
+            T.g.copy_(to_dev(g, torch.bfloat16))
+        M.mp_adamw_step([T.param() for T in Ts], ghp, st)
+        O.adamw_step(ohp, ost, [T.oracle_tuple(g) for T, g in zip(Ts, hosts)], O.BF16, O.BF16)
+        torch.cuda.synchronize()
+        assert_state_equal(M.read_scaler_state(st), ost)
+        for i in (0, 1, 511, 512, 513, 599):
+            Ts[i].compare(f"step {k} tensor {i}")
+    assert ost.found_inf == 1 and ost.step == 1
+
+
+def test_empty_parameter_list_still_counts_the_step():
+    ghp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    st = M.new_scaler_state(8.0)
+    M.mp_adamw_step([], ghp, st, grad_dtype=M.MP_F16, working_dtype=M.MP_F16)
+    s = M.read_scaler_state(st)
+    assert s.step == 1 and s.found_inf == 0
+
+
+def test_invalid_arguments_are_rejected_before_launch():
+    ghp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    st = M.new_scaler_state()
+    w = torch.zeros(9, dtype=torch.float32, device="cuda")
+    g = torch.zeros(9, dtype=torch.float16, device="cuda")
+    before = M.mp_launch_count()
+    with pytest.raises(M.MpError) as e:
+        M.mp_adamw_step([M.Param(w[1:], w[1:], w[1:], g[1:], g[1:])], ghp, st)
+    assert e.value.status == M.MP_EALIGN
+    with pytest.raises(M.MpError) as e:
+        M.mp_adamw_step([M.Param(w, w, w, g, g)], M.AdamwHparams(1e-3, 1.0, 0.999, 1e-8, 0.0), st)
+    assert e.value.status == M.MP_EINVAL
+    with pytest.raises(M.MpError):
+        M.loss_scale_update(st, M.ScalerCfg(2.0, 0.5, 0, 1))
+    assert M.mp_launch_count() == before
+
+
+def test_full_model_step_sampled():
+    """Llama-3-8B-shaped list, 290 tensors, 8.03e9 params, 5 steps with an inf
+    on step 3: found_inf per step against torch's isfinite over every grad,
+    the working copy against torch's BF16 rounding of every master element,
+    and sampled elements of every tensor against the oracle."""
+    c = W.FULL
+    params = W.llama3_8b_params()
+    total = sum(n for _, n in params)
+    free, _ = torch.cuda.mem_get_info()
+    need = total * 16 + (4 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free, have {free / 2**30:.0f}")
+    ghp, ohp = hp_of(c)
+    cfg, ocfg = M.ScalerCfg(c.growth, c.backoff, c.interval, 1), O.ScalerCfg(c.growth, c.backoff, c.interval, 1)
+    ws, ms, vs, gs, w16s = [], [], [], [], []
+    for t, (name, n) in enumerate(params):
+        w = torch.empty(n, dtype=torch.float32, device="cuda")
+        synth.fill_device(c.master_recipe(t), synth.F32, w)
+        ws.append(w)
+        ms.append(torch.zeros(n, dtype=torch.float32, device="cuda"))
+        vs.append(torch.zeros(n, dtype=torch.float32, device="cuda"))
+        gs.append(torch.empty(n, dtype=torch.float16, device="cuda"))
+        w16s.append(torch.empty(n, dtype=torch.bfloat16, device="cuda"))
+    plist = [M.Param(ws[i], ms[i], vs[i], gs[i], w16s[i]) for i in range(len(params))]
+    rng = np.random.default_rng(7)
+    inf_t = [nm for nm, _ in params].index(c.inf_tensor)
+    samples = []
+    for t, (name, n) in enumerate(params):
+        idx = np.unique(np.concatenate([rng.integers(0, n, 96), np.arange(min(n, 8)), np.arange(max(0, n - 8), n),
+                                        [c.inject_index] if t == inf_t else []]).astype(np.int64))
+        samples.append(idx)
+    ostate = O.new_scaler_state(c.scale)
+    st = M.new_scaler_state(c.scale)
+    ow = [synth.fill_at(c.master_recipe(t), synth.F32, idx) for t, idx in enumerate(samples)]
+    om = [np.zeros(i.size, np.float32) for i in samples]
+    ov = [np.zeros(i.size, np.float32) for i in samples]
+    ow16 = [np.zeros(i.size, np.uint16) for i in samples]
+    for step in range(1, c.steps + 1):
+        for t, (name, n) in enumerate(params):
+            synth.fill_device(c.grad_recipe(t, step), synth.F16, gs[t])
+        if step == c.inf_step:
+            gs[inf_t][c.inject_index] = float("inf")
+        found = int(any(bool((~torch.isfinite(g)).any().item()) for g in gs))
+        M.mp_adamw_step(plist, ghp, st)
+        M.loss_scale_update(st, cfg)
+        s_orc = O.adamw_begin(ohp, ostate, found)
+        if not found:
+            for t, idx in enumerate(samples):
+                g_s = synth.fill_at(c.grad_recipe(t, step), synth.F16, idx)
+                O.adamw_apply(s_orc, ow[t], om[t], ov[t], g_s, O.F16, ow16[t], O.BF16)
+        O.loss_scale_update(ostate, ocfg)
+        torch.cuda.synchronize()
+        gst = M.read_scaler_state(st)
+        assert gst.found_inf == found == int(step == c.inf_step)
+        assert_state_equal(gst, ostate)
+    for t, idx in enumerate(samples):
+        it = torch.from_numpy(idx).cuda()
+        for gt, ot, nm in ((ws[t], ow[t], "w"), (ms[t], om[t], "m"), (vs[t], ov[t], "v")):
+            d = ulp_diff(gt[it].cpu().numpy(), ot)
+            assert d.max() <= MAX_ULP, f"{params[t][0]} {nm}: {d.max()} ulp"
+            assert d.max() == 0, f"{params[t][0]} {nm}: {d.max()} ulp (within tolerance, not exact)"
+        np.testing.assert_array_equal(to_host(w16s[t][it], np.uint16), ow16[t])
+        assert bool((ws[t].to(torch.bfloat16).view(torch.int16) == w16s[t].view(torch.int16)).all().item()), \
+            f"{params[t][0]}: working copy is not the RNE of the master"
+    assert M.read_scaler_state(st).step == c.steps - 1

@@ -1,0 +1,103 @@
+"""CPU tests of the host side: the C ABI library loads and exports every
+entry point declared in include/mpnum.h, its structs match the binding, its
+host-only helpers and argument validation work without a GPU, and the
+parallel oracle driver used by the GPU tests equals the plain oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synth
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "mpnum.h")
+
+
+@pytest.fixture(scope="module")
+def M():
+    from mixed_precision_numerics_gb300 import build
+
+    build.build()
+    import mixed_precision_numerics_gb300 as pkg
+
+    return pkg
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"MP_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(M):
+    names = declared_functions()
+    assert {"mp_adamw_step", "loss_scale_update", "fp8_cast_delayed", "nvfp4_quantize", "rht16"} <= set(names)
+    raw = ctypes.CDLL(M.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), f"{n} declared in mpnum.h but not exported"
+
+
+def test_struct_layouts(M):
+    st = M.ScalerState()
+    M.lib.mp_scaler_state_init(ctypes.byref(st), 65536.0)
+    assert st.scale == 65536.0 and st.beta1_pow == 1.0 and st.beta2_pow == 1.0 and st.step == 0
+    assert ctypes.sizeof(M.ScalerState) == 88 and M.ScalerState.internal_found.offset == 48
+    m = M.Fp8Meta()
+    M.lib.mp_fp8_meta_init(ctypes.byref(m))
+    assert (m.scale, m.scale_inv, m.amax, m.pos) == (1.0, 1.0, 0.0, 0)
+    assert M.nvfp4_workspace_size() >= 8
+    for s in (0, -1, -2, -3, -4, -5):
+        assert M.mp_status_str(s)
+
+
+def test_argument_validation_without_gpu(M):
+    L = M.lib
+    hp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
+    assert L.mp_adamw_step(None, 0, 9, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EINVAL
+    assert L.mp_adamw_step(None, -1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EINVAL
+    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(hp), 12, None) == M.MP_EALIGN
+    bad = M.AdamwHparams(float("nan"), 0.9, 0.999, 1e-8, 0.0)
+    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(bad), 16, None) == M.MP_EINVAL
+    p = (M.MpParam * 1)(M.MpParam(16, 16, 16, 24, 16, 5))
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EALIGN
+    cfg = M.ScalerCfg(2.0, 0.5, 0, 1)
+    assert L.loss_scale_update(16, ctypes.byref(cfg), None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_F16, 16, 16, 4, 1.0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 0, 1.0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 0.0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(8, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, None) == M.MP_EALIGN
+    q = L.nvfp4_quantize
+    assert q(16, 2, 24, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
+    assert q(16, 8, 32, 1, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
+    assert q(16, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 4, None) == M.MP_EWORKSPACE
+    assert q(8, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_EALIGN
+    assert L.rht16(16, 2, 40, 0, 16, M.MP_F32, None) == M.MP_ESHAPE
+    assert L.rht16(16, 2, 32, 0, 16, M.MP_E4M3, None) == M.MP_EINVAL
+    assert M.mp_launch_count() == 0
+
+
+@pytest.mark.parametrize("b2,sr,rht", [(False, False, False), (False, True, True), (True, False, True), (True, True, False)])
+def test_parallel_oracle_driver_equals_plain_oracle(b2, sr, rht):
+    from tests.gpu_util import nvfp4_oracle
+
+    x = synth.fill(synth.recipe(3, 0, 1.0, 0.01, 30.0, synth.OUT_SCALE), synth.BF16, 400 * 320, shape=(400, 320))
+    x = x[:384] if b2 else x
+    a = nvfp4_oracle(x, b2, sr, 42, rht, 0x1234)
+    b = O.nvfp4_quantize(x, b2, sr, 42, rht, 0x1234)
+    for u, v in zip(a, b):
+        if isinstance(u, np.ndarray):
+            np.testing.assert_array_equal(u, v)
+        else:
+            assert u == v
+
+
+def test_generator_is_deterministic_and_reproducible_by_index():
+    r = synth.recipe(9, 3, 2.0, 0.01, 10.0, synth.OUT_SCALE)
+    a = synth.fill(r, synth.F16, 5000)
+    b = synth.fill(r, synth.F16, 5000)
+    np.testing.assert_array_equal(a, b)
+    idx = np.array([0, 17, 4999])
+    np.testing.assert_array_equal(synth.fill_at(r, synth.F16, idx), a[idx])
+    np.testing.assert_array_equal(synth.fill(r, synth.F16, 10, start=17), a[17:27])

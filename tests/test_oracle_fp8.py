@@ -107,3 +107,11 @@ def test_cast_matches_torch_inside_range(fmt):
     assert sat.any()
     np.testing.assert_array_equal(y[sat], np.where(p[sat] > 0, 0x7E if fmt == O.E4M3 else 0x7B,
                                                    0xFE if fmt == O.E4M3 else 0xFB))
+
+
+def test_ring_slot_is_taken_modulo_the_length():
+    meta = O.new_fp8_meta()
+    meta.pos = 9
+    hist = np.zeros(4, np.float32)
+    O.fp8_cast_delayed(one_hot(32, 0, 5.0), O.BF16, O.E4M3, meta, hist, 1.0)
+    assert hist[1] == 5.0 and meta.pos == 2
