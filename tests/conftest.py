@@ -14,6 +14,11 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
     config.addinivalue_line("markers", "slow: long-running CPU test")
+    # Build the CUDA library, the input generator and the oracle up front
+    # (no-ops when up to date), so that every test module can import them.
+    import __graft_entry__
+
+    __graft_entry__.build()
 
 
 def golden(name):

@@ -16,7 +16,7 @@ from tests.gpu_util import to_dev, to_host, ulp_diff
 
 pytestmark = pytest.mark.gpu
 
-M = pytest.importorskip("mixed_precision_numerics_gb300")
+import mixed_precision_numerics_gb300 as M  # noqa: E402
 TD = {O.F16: torch.float16, O.BF16: torch.bfloat16}
 MPD = {O.F16: M.MP_F16, O.BF16: M.MP_BF16}
 MAX_ULP = 4
@@ -240,3 +240,22 @@ def test_full_model_step_sampled():
         assert bool((ws[t].to(torch.bfloat16).view(torch.int16) == w16s[t].view(torch.int16)).all().item()), \
             f"{params[t][0]}: working copy is not the RNE of the master"
     assert M.read_scaler_state(st).step == c.steps - 1
+
+
+def test_check_then_apply_equals_fused_step():
+    n = 50_001
+    ghp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.01)
+    w0 = synth.fill(synth.recipe(40, 0, 0.02), synth.F32, n)
+    A, B = Tensors(w0, O.F16, O.BF16), Tensors(w0, O.F16, O.BF16)
+    sa, sb = M.new_scaler_state(512.0), M.new_scaler_state(512.0)
+    for k in range(3):
+        g = to_dev(synth.fill(synth.recipe(41, k, 5.0), synth.F16, n), torch.float16)
+        A.g.copy_(g)
+        B.g.copy_(g)
+        M.mp_adamw_step([A.param()], ghp, sa)
+        M.mp_adamw_check([B.param()], ghp, sb)
+        M.mp_adamw_apply([B.param()], ghp, sb)
+    torch.cuda.synchronize()
+    for x, y in ((A.w, B.w), (A.m, B.m), (A.v, B.v), (A.w16, B.w16)):
+        assert torch.equal(x.view(torch.int8) if x.dtype != torch.float32 else x, y.view(torch.int8) if y.dtype != torch.float32 else y)
+    assert bytes(M.read_scaler_state(sa)) == bytes(M.read_scaler_state(sb))

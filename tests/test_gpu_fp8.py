@@ -19,7 +19,7 @@ from tests.gpu_util import to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
-M = pytest.importorskip("mixed_precision_numerics_gb300")
+import mixed_precision_numerics_gb300 as M  # noqa: E402
 FMT = {M.MP_E4M3: O.E4M3, M.MP_E5M2: O.E5M2}
 XFMT = {torch.float32: O.F32, torch.float16: O.F16, torch.bfloat16: O.BF16}
 

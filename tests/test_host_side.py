@@ -18,9 +18,9 @@ HEADER = os.path.join(ROOT, "include", "mpnum.h")
 
 @pytest.fixture(scope="module")
 def M():
-    from mixed_precision_numerics_gb300 import build
+    import __graft_entry__
 
-    build.build()
+    __graft_entry__._package_builder().build()
     import mixed_precision_numerics_gb300 as pkg
 
     return pkg
