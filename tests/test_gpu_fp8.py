@@ -180,6 +180,13 @@ def test_fp8_workload_full_size_sampled(which):
         assert np.array_equal(y_s, ref), f"iteration {k}"
         O.fp8_history_update(om, oh, c.margin, amax, FMT[fmt])
         assert_meta_equal(M.read_fp8_meta(meta), om)
-        sat += int(np.count_nonzero((ref & 0x7F) == (0x7E if fmt == M.MP_E4M3 else 0x7B)))
+        # Whole-tensor property: a byte is the largest code exactly when
+        # |x * scale| rounds to it or beyond (the tie at the midpoint below the
+        # top goes to the even code: up for E4M3, down for E5M2).
+        p = (x.float() * scale_in_force).abs()
+        top = (y & 0x7F) == (0x7E if fmt == M.MP_E4M3 else 0x7B)
+        expect = (p >= 432.0) if fmt == M.MP_E4M3 else (p > 53248.0)
+        assert torch.equal(top, expect), f"iteration {k}: saturation pattern"
+        sat += int(top.sum().item())
     if which == "act":
         assert sat > 0  # the drifting std makes the delayed scale lag: saturation happens
