@@ -232,6 +232,32 @@ MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, 
                                 float* d_tensor_scale, int32_t* d_nonfinite, void* dequant_bf16,
                                 void* d_workspace, size_t workspace_bytes, void* stream);
 
+/* nvfp4_quantize_noalloc — nvfp4_quantize without a caller-supplied
+ * workspace.  The pages describe nothing like it: it exists for callers that
+ * cannot allocate device memory at the point of the call, for example code
+ * running inside a framework step whose memory pool must not grow, plugin
+ * interfaces that are handed only their inputs and outputs, or host code that
+ * must avoid cudaMalloc because it synchronises the device.  Arguments,
+ * outputs and results are those of nvfp4_quantize.  The scratch is a
+ * file-scope device array of nvfp4_noalloc_scratch_bytes() (256) bytes that
+ * every device holds from library load to process exit; a call needs
+ * nvfp4_workspace_size() bytes of it and returns MP_EWORKSPACE if that is
+ * more than the array holds.  The call allocates and frees nothing.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current: make that first call
+ * before any stream capture.  Each call first clears the words that must
+ * start at zero (a stream-ordered memset of the library's own scratch; this
+ * happens before the argument checks, which otherwise behave as in
+ * nvfp4_quantize).  Every call on a device shares the one array: calls that
+ * overlap on the GPU (different streams, no ordering between them) race on it
+ * and their results are undefined. */
+MP_API size_t nvfp4_noalloc_scratch_bytes(void);
+MP_API mp_status nvfp4_quantize_noalloc(const void* x_bf16, int64_t rows, int64_t cols,
+                                        int32_t block_2d, int32_t stochastic, uint64_t seed,
+                                        int32_t apply_rht, uint16_t rht_sign_mask, uint8_t* codes,
+                                        uint8_t* block_scales, float* d_tensor_scale,
+                                        int32_t* d_nonfinite, void* dequant_bf16, void* stream);
+
 /* rht16 — the 16-point random Hadamard transform ([NVFP4] §2.2 item 2):
  * for every 16 contiguous elements t of each row of BF16 x [rows, cols],
  * y_t = 1/4 * H16 * diag(s) * x_t, H16 the Sylvester Hadamard matrix

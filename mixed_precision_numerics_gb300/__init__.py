@@ -100,6 +100,8 @@ def _load() -> ctypes.CDLL:
         "nvfp4_workspace_size": (S, []),
         "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
         "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
+        "nvfp4_noalloc_scratch_bytes": (S, []),
+        "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -277,6 +279,20 @@ def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *
                               workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
+def nvfp4_quantize_noalloc(x, codes, block_scales, tensor_scale, nonfinite, *, block_2d: bool = False,
+                           stochastic: bool = False, seed: int = 0, apply_rht: bool = False, sign_mask: int = 0,
+                           dequant=None, rows: int | None = None, cols: int | None = None, stream=None) -> None:
+    """nvfp4_quantize for callers that cannot allocate a workspace: the
+    library's own fixed device scratch is used instead (calls that overlap
+    on the GPU race on it; see the C header)."""
+    if rows is None:
+        rows, cols = x.shape
+    _check("nvfp4_quantize_noalloc",
+           lib.nvfp4_quantize_noalloc(_ptr(x), rows, cols, int(block_2d), int(stochastic), seed & (2**64 - 1),
+                                      int(apply_rht), sign_mask & 0xFFFF, _ptr(codes), _ptr(block_scales),
+                                      _ptr(tensor_scale), _ptr(nonfinite), _ptr(dequant), _stream(stream)))
+
+
 def rht16(x, y, sign_mask: int, stream=None) -> None:
     rows, cols = x.shape
     _check("rht16", lib.rht16(_ptr(x), rows, cols, sign_mask & 0xFFFF, _ptr(y), _dtype_code(y), _stream(stream)))
@@ -285,7 +301,7 @@ def rht16(x, y, sign_mask: int, stream=None) -> None:
 __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
-    "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "loss_scale_update", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
+    "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "loss_scale_update", "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",
     "make_param_array",

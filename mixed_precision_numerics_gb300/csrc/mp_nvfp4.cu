@@ -17,6 +17,8 @@
 //                   per block.
 // The transform is evaluated on CUDA cores by the butterfly in binary32 so
 // that its additions happen in the documented order.
+#include <mutex>
+
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -401,3 +403,60 @@ MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// nvfp4_quantize_noalloc: the same quantiser for callers that cannot hand the
+// library a workspace.  Its scratch is this file-scope device array, created
+// when the library is loaded on each device and kept until the process exits.
+// Host code may not take the array's address directly (the name is a host-side
+// stand-in); the device address is looked up once per device with
+// cudaGetSymbolAddress, with that device current.
+// ---------------------------------------------------------------------------
+namespace mp {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256;
+__device__ __align__(256) unsigned char g_nvfp4_noalloc_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+mp_status noalloc_scratch_for_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MP_ECUDA;
+  if (dev < 0 || dev >= kMaxDevices) return MP_EINVAL;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_nvfp4_noalloc_scratch) != cudaSuccess || !p) return MP_ECUDA;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return MP_OK;
+}
+
+}  // namespace
+}  // namespace mp
+
+extern "C" MP_API size_t nvfp4_noalloc_scratch_bytes(void) { return mp::kNoAllocScratchBytes; }
+
+extern "C" MP_API mp_status nvfp4_quantize_noalloc(const void* x_bf16, int64_t rows, int64_t cols,
+                                                   int32_t block_2d, int32_t stochastic, uint64_t seed,
+                                                   int32_t apply_rht, uint16_t rht_sign_mask, uint8_t* codes,
+                                                   uint8_t* block_scales, float* d_tensor_scale,
+                                                   int32_t* d_nonfinite, void* dequant_bf16, void* stream) {
+  using namespace mp;
+  // A call needs nvfp4_workspace_size() bytes of scratch; the fixed array
+  // must hold that much.
+  if (nvfp4_workspace_size() > kNoAllocScratchBytes) return MP_EWORKSPACE;
+  void* scratch = nullptr;
+  const mp_status rc = noalloc_scratch_for_current_device(&scratch);
+  if (rc != MP_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // The accumulator and ticket must start at zero; clear them in stream order.
+  if (cudaMemsetAsync(scratch, 0, sizeof(Ws), s) != cudaSuccess) return MP_ECUDA;
+  return nvfp4_quantize(x_bf16, rows, cols, block_2d, stochastic, seed, apply_rht, rht_sign_mask, codes,
+                        block_scales, d_tensor_scale, d_nonfinite, dequant_bf16, scratch, kNoAllocScratchBytes,
+                        stream);
+}
