@@ -94,7 +94,7 @@ typedef struct {
   float scale;            /* loss scale S in force for the next step */
   int32_t growth_tracker; /* consecutive clean steps since the last change */
   int32_t found_inf;      /* 1 if the most recent step saw an inf/NaN grad */
-  int32_t reserved0;
+  int32_t error_flags;    /* nonzero if a kernel of a step gave up a bounded wait; outputs undefined */
   int64_t step;           /* applied (not skipped) optimizer steps */
   double beta1_pow;       /* beta1^step */
   double beta2_pow;       /* beta2^step */

@@ -42,7 +42,7 @@ class ScalerState(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("growth_tracker", ctypes.c_int32),
         ("found_inf", ctypes.c_int32),
-        ("reserved0", ctypes.c_int32),
+        ("error_flags", ctypes.c_int32),
         ("step", ctypes.c_int64),
         ("beta1_pow", ctypes.c_double),
         ("beta2_pow", ctypes.c_double),
