@@ -291,6 +291,39 @@ class Workload:
                              stochastic=q["sr"], seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"])
             rec(6 + i)
 
+    def isolated_call_times(self, reps: int = 16) -> dict:
+        """Microseconds per call of each FP8 / NVFP4 call, replayed from a CUDA graph."""
+        torch, M = self.torch, self.M
+        calls = {
+            "fp8_act_e4m3": lambda k: M.fp8_cast_delayed(self.act[k % self.nbuf], self.y_act, M.MP_E4M3,
+                                                         self.meta_act, self.hist_act, self.fp8_margin),
+            "fp8_grad_e5m2": lambda k: M.fp8_cast_delayed(self.grd[k % self.nbuf], self.y_grd, M.MP_E5M2,
+                                                          self.meta_grd, self.hist_grd, self.fp8_margin),
+        }
+        for q in self.q:
+            calls[q["name"]] = (lambda q: lambda k: M.nvfp4_quantize(
+                q["x"], q["codes"], q["scales"], q["ts"], q["nf"], q["ws"], block_2d=q["b2"], stochastic=q["sr"],
+                seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"]))(q)
+        clean = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        out = {}
+        for name, fn in calls.items():
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    for k in range(reps):
+                        fn(k)
+            torch.cuda.current_stream().wait_stream(side)
+            clean.sum()  # read-only pass: leaves L2 holding clean lines
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            out[name] = a.elapsed_time(b) * 1e3 / reps
+        return out
+
     # ---- end to end through host buffers -------------------------------------------------
     def e2e_setup(self):
         torch = self.torch
@@ -542,6 +575,16 @@ def main():
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
                 "traffic": round(tpp * wl.P) if tpp else None}
+
+    # Each quantiser call alone: 16 back-to-back calls captured in a CUDA
+    # graph and replayed after an L2-clean point, so neither launch gaps nor
+    # the previous kernel's dirty L2 lines are charged to it.
+    isolated = wl.isolated_call_times() if not args.small else {}
+    for name, us in isolated.items():
+        gbs = wl.bytes[name] / (us * 1e-6) / 1e9
+        kernels[name]["graph_isolated_us"] = round(us, 2)
+        kernels[name]["graph_isolated_gbs"] = round(gbs, 1)
+        kernels[name]["graph_isolated_frac_of_" + peak_kind + "_hbm"] = round(gbs / peak, 4)
 
     e2e = None
     if not args.no_e2e:

@@ -174,7 +174,8 @@ typedef struct {
   /* library-internal: zero after mp_fp8_meta_init, left zero between calls */
   uint32_t internal_amax;
   uint32_t internal_ticket;
-  uint32_t reserved[2];
+  uint32_t internal_hrest;
+  uint32_t reserved;
 } mp_fp8_meta;
 
 /* Host helper: scale = scale_inv = 1, amax = 0, pos = 0, internals zero. */

@@ -70,7 +70,8 @@ class Fp8Meta(ctypes.Structure):
         ("pos", ctypes.c_int32),
         ("internal_amax", ctypes.c_uint32),
         ("internal_ticket", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32 * 2),
+        ("internal_hrest", ctypes.c_uint32),
+        ("reserved", ctypes.c_uint32),
     ]
 
 

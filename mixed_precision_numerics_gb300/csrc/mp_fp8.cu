@@ -6,10 +6,12 @@
 // (x_fp8 = clip(x/s, -448, 448)), "E4M3 vs E5M2" (E4M3 forward, E5M2 grads).
 //
 // k_fp8_cast: every thread streams 16 input elements per vector (32 B of
-// BF16/F16, 64 B of F32) and writes 16 output bytes, keeping a running
-// NaN-propagating max |x| in a register.  CTAs fold their amax into the meta
-// word with one atomicMax each; the last CTA to finish (atomic ticket, no
-// waiting) writes the ring slot and derives the next scale.
+// BF16/F16, 64 B of F32), 128 B of input in flight, and writes 16 output bytes
+// per vector, keeping a running NaN-propagating max |x| in a register.  CTAs
+// fold their amax into the meta word with one atomicMax each; CTA 0 folds the
+// history entries the call does not overwrite while the stream runs; the last
+// CTA to finish (atomic ticket, no waiting) writes the ring slot and derives
+// the next scale from the two maxima.
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -18,31 +20,38 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kElems = 16;  // elements per vector
-constexpr int kUnroll = 2;
 
 enum { XF32 = 0, XF16 = 1, XBF16 = 2 };
 
+// Vectors in flight per thread: 128 bytes of input either way.
 template <int XT>
-__device__ __forceinline__ void load16(const void* x, int64_t vec, float (&f)[16]) {
+__host__ __device__ constexpr int unroll_of() { return XT == XF32 ? 2 : 4; }
+
+// Raw 16-element vector: two 16-byte words of 16-bit values, or four of FP32.
+template <int XT>
+__device__ __forceinline__ void load_raw(const void* x, int64_t vec, uint4 (&r)[4]) {
   if constexpr (XT == XF32) {
-    const float* p = static_cast<const float*>(x) + vec * kElems;
+    const uint4* p = static_cast<const uint4*>(x) + vec * 4;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float4 q = ld_cs_f4(p + 4 * k);
-      f[4 * k] = q.x;
-      f[4 * k + 1] = q.y;
-      f[4 * k + 2] = q.z;
-      f[4 * k + 3] = q.w;
-    }
+    for (int k = 0; k < 4; ++k) r[k] = __ldcs(p + k);
   } else {
-    const uint16_t* p = static_cast<const uint16_t*>(x) + vec * kElems;
-    const uint4 a = ld_cs(p), b = ld_cs(p + 8);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      f[2 * k] = XT == XBF16 ? bf16lo(w[k]) : f16lo(w[k]);
-      f[2 * k + 1] = XT == XBF16 ? bf16hi(w[k]) : f16hi(w[k]);
-    }
+    const uint4* p = static_cast<const uint4*>(x) + vec * 2;
+    r[0] = __ldcs(p);
+    r[1] = __ldcs(p + 1);
+  }
+}
+
+// Element pair k (elements 2k, 2k+1) of a raw vector as floats.
+template <int XT>
+__device__ __forceinline__ float2 pair_of(const uint4 (&r)[4], int k) {
+  if constexpr (XT == XF32) {
+    const uint4 q = r[k >> 1];
+    return (k & 1) ? make_float2(__uint_as_float(q.z), __uint_as_float(q.w))
+                   : make_float2(__uint_as_float(q.x), __uint_as_float(q.y));
+  } else {
+    const uint4 q = r[k >> 2];
+    const uint32_t w = (k & 3) == 0 ? q.x : (k & 3) == 1 ? q.y : (k & 3) == 2 ? q.z : q.w;
+    return XT == XBF16 ? make_float2(bf16lo(w), bf16hi(w)) : make_float2(f16lo(w), f16hi(w));
   }
 }
 
@@ -63,42 +72,64 @@ __device__ __forceinline__ uint32_t cast_pair(float p0, float p1) {
   return E5M2 ? cvt_e5m2x2(p0, p1) : cvt_e4m3x2(p0, p1);
 }
 
+// Ordered key of a history entry: NaN above everything, non-positive as 0.
+__device__ __forceinline__ uint32_t hist_key(float h) {
+  return (h != h) ? 0x7FC00000u : (h > 0.0f ? __float_as_uint(h) : 0u);
+}
+
 template <int XT, bool E5M2>
 __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ x, int64_t n,
                                                        uint8_t* __restrict__ y, mp_fp8_meta* meta,
                                                        float* hist, int32_t hist_len, float margin) {
+  constexpr int U = unroll_of<XT>();
   __shared__ uint32_t red[32];
   __shared__ int is_last;
   const float scale = meta->scale;
+  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
+
+  // CTA 0 folds the history entries this call does not overwrite while the
+  // stream runs, so the last CTA only has to combine them with this amax.
+  if (blockIdx.x == 0) {
+    uint32_t hm = 0;
+    for (int i = threadIdx.x; i < hist_len; i += kThreads)
+      if (i != slot) hm = max(hm, hist_key(hist[i]));
+    hm = block_max_u32(hm, red);
+    if (threadIdx.x == 0) meta->internal_hrest = hm;
+    __syncthreads();  // red is reused below
+  }
+
   float acc = 0.0f;
   const int64_t nvec = n / kElems;
-  const int64_t step = (int64_t)gridDim.x * kThreads * kUnroll;
-  for (int64_t v0 = (int64_t)blockIdx.x * kThreads * kUnroll + threadIdx.x; v0 < nvec; v0 += step) {
-    float f[kUnroll][16];
+  const int64_t step = (int64_t)gridDim.x * kThreads * U;
+  for (int64_t v0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; v0 < nvec; v0 += step) {
+    uint4 raw[U][4];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t vec = v0 + (int64_t)u * kThreads;
-      if (vec < nvec) load16<XT>(x, vec, f[u]);
+      if (vec < nvec) load_raw<XT>(x, vec, raw[u]);
     }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
+    for (int u = 0; u < U; ++u) {
       const int64_t vec = v0 + (int64_t)u * kThreads;
       if (vec >= nvec) continue;
       float vmax = 0.0f;
       uint32_t h[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        const float a = f[u][2 * k], b = f[u][2 * k + 1];
-        vmax = max_abs_nan(vmax, a);
-        vmax = max_abs_nan(vmax, b);
-        h[k] = cast_pair<E5M2>(__fmul_rn(a, scale), __fmul_rn(b, scale));
+        const float2 f = pair_of<XT>(raw[u], k);
+        vmax = max_abs_nan(vmax, f.x);
+        vmax = max_abs_nan(vmax, f.y);
+        h[k] = cast_pair<E5M2>(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
       }
       uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
       if (__builtin_expect(vmax != vmax, 0)) {  // a NaN input: its byte is 0x7F
         uint8_t* ob = reinterpret_cast<uint8_t*>(&o);
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          if (f[u][j] != f[u][j]) ob[j] = 0x7F;
+        for (int k = 0; k < 8; ++k) {
+          const float2 f = pair_of<XT>(raw[u], k);
+          if (f.x != f.x) ob[2 * k] = 0x7F;
+          if (f.y != f.y) ob[2 * k + 1] = 0x7F;
+        }
       }
       st_cs(y + vec * kElems, o);
       acc = max_abs_nan(acc, vmax);
@@ -123,36 +154,25 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
     is_last = atomicAdd(&meta->internal_ticket, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!is_last) return;
+  if (!is_last || threadIdx.x != 0) return;
 
   // Last CTA: record this step's amax and derive the next scale.
   __threadfence();
-  if (threadIdx.x == 0) {
-    const uint32_t ab = atomicExch(&meta->internal_amax, 0u);
-    meta->internal_ticket = 0;
-    const float amax = __uint_as_float(ab);
-    const int32_t pos = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
-    meta->amax = amax;
-    hist[pos] = amax;
-    meta->pos = (pos + 1) % hist_len;
-  }
-  __syncthreads();
-  uint32_t hm = 0;
-  for (int i = threadIdx.x; i < hist_len; i += kThreads) {
-    const float h = hist[i];
-    hm = max(hm, (h != h) ? 0x7FC00000u : (h > 0.0f ? __float_as_uint(h) : 0u));
-  }
-  hm = block_max_u32(hm, red);
-  if (threadIdx.x == 0) {
-    const float H = __uint_as_float(hm);
-    if (isfinite(H) && H > 0.0f) {
-      const float denom = __fmul_rn(margin, H);
-      if (isfinite(denom) && denom > 0.0f) {
-        const float ns = __fdiv_rn(E5M2 ? 57344.0f : 448.0f, denom);
-        if (isfinite(ns) && ns > 0.0f) {
-          meta->scale = ns;
-          meta->scale_inv = __fdiv_rn(1.0f, ns);
-        }
+  const uint32_t ab = atomicExch(&meta->internal_amax, 0u);
+  const uint32_t hm = max(*reinterpret_cast<volatile uint32_t*>(&meta->internal_hrest), ab);
+  meta->internal_ticket = 0;
+  const float amax = __uint_as_float(ab);
+  meta->amax = amax;
+  hist[slot] = amax;
+  meta->pos = (slot + 1) % hist_len;
+  const float H = __uint_as_float(hm);
+  if (isfinite(H) && H > 0.0f) {
+    const float denom = __fmul_rn(margin, H);
+    if (isfinite(denom) && denom > 0.0f) {
+      const float ns = __fdiv_rn(E5M2 ? 57344.0f : 448.0f, denom);
+      if (isfinite(ns) && ns > 0.0f) {
+        meta->scale = ns;
+        meta->scale_inv = __fdiv_rn(1.0f, ns);
       }
     }
   }
@@ -169,7 +189,8 @@ mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float*
     occ = o;
   }
   const int64_t nvec = n / kElems;
-  const int64_t ctas = (nvec + (int64_t)kThreads * kUnroll - 1) / ((int64_t)kThreads * kUnroll);
+  constexpr int U = unroll_of<XT>();
+  const int64_t ctas = (nvec + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
   k_fp8_cast<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin);
   note_launches(1);
   return launch_status();
