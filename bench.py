@@ -291,6 +291,22 @@ class Workload:
                              stochastic=q["sr"], seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"])
             rec(6 + i)
 
+    def clipped_check_ms(self, reps: int = 5) -> float:
+        """The check pass with gradient-norm clipping (max norm 1.0) on the same
+        parameter list: tile sums of g*g plus the one-CTA fold."""
+        torch, M = self.torch, self.M
+        hp = M.AdamwHparams(self.hp.lr, self.hp.beta1, self.hp.beta2, self.hp.eps, self.hp.weight_decay, 1.0)
+        ws = torch.empty(M.mp_adamw_workspace_size(self.params), dtype=torch.uint8, device="cuda")
+        state = M.new_scaler_state(65536.0)
+        M.mp_adamw_check(self.params, hp, state, grad_dtype=M.MP_F16, workspace=ws)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * reps)]
+        for k in range(reps):
+            ev[2 * k].record()
+            M.mp_adamw_check(self.params, hp, state, grad_dtype=M.MP_F16, workspace=ws)
+            ev[2 * k + 1].record()
+        torch.cuda.synchronize()
+        return statistics.median(ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(reps))
+
     def isolated_call_times(self, reps: int = 16) -> dict:
         """Microseconds per call of each FP8 / NVFP4 call, replayed from a CUDA graph."""
         torch, M = self.torch, self.M
@@ -585,6 +601,12 @@ def main():
         kernels[name]["graph_isolated_us"] = round(us, 2)
         kernels[name]["graph_isolated_gbs"] = round(gbs, 1)
         kernels[name]["graph_isolated_frac_of_" + peak_kind + "_hbm"] = round(gbs / peak, 4)
+
+    clip_ms = wl.clipped_check_ms()
+    gbs = wl.bytes["adamw_check"] / (clip_ms * 1e-3) / 1e9
+    kernels["adamw_check_with_clipping"] = {"ms": round(clip_ms, 4), "bytes": int(wl.bytes["adamw_check"]),
+                                            "gbs": round(gbs, 1), "frac_of_" + peak_kind + "_hbm": round(gbs / peak, 4),
+                                            "note": "not in the step: max_grad_norm 1.0, timed after it"}
 
     e2e = None
     if not args.no_e2e:

@@ -82,9 +82,12 @@ typedef struct {
   int64_t numel;
 } mp_param;
 
-/* AdamW hyperparameters ([MPT-ko] "FP16 학습 루프": AdamW, lr 1e-3). */
+/* AdamW hyperparameters ([MPT-ko] "FP16 학습 루프": AdamW, lr 1e-3, and
+ * clip_grad_norm_(max_norm=1.0) after unscale_).  max_grad_norm > 0 clips the
+ * unscaled grads to that global L2 norm; 0 disables clipping. */
 typedef struct {
   float lr, beta1, beta2, eps, weight_decay;
+  float max_grad_norm;
 } mp_adamw_hparams;
 
 /* Device-resident state of the loss scaler and the step counter, 88 bytes.
@@ -99,10 +102,12 @@ typedef struct {
   double beta1_pow;       /* beta1^step */
   double beta2_pow;       /* beta2^step */
   int64_t skipped;        /* steps skipped because of inf/NaN */
+  float grad_norm;        /* global L2 norm of the unscaled grads (-1 without clipping) */
+  float clip_coef;        /* factor applied to the unscaled grads (1 without clipping) */
   /* library-internal: zero after mp_scaler_state_init, left zero between calls */
   uint32_t internal_found;
   uint32_t internal_ticket;
-  float internal_scalars[8];
+  float internal_scalars[6];
 } mp_scaler_state;
 
 /* Loss-scale schedule ([MPT-ko] "손실 스케일링": GradScaler defaults 65536,
@@ -126,29 +131,44 @@ MP_API void mp_scaler_state_init(mp_scaler_state* host_state, float init_scale);
  * ([MPT-ko]: the update of that step is skipped).  Otherwise step += 1, the
  * beta powers advance and every element is updated, in binary32, with
  * scalars formed once per step in binary64 from the float hyperparameters:
- *     g  = fp32(grad) * (1/S)                      unscale
+ *     g  = (fp32(grad) * (1/S)) * clip             unscale, then clip
  *     w  = w * (1 - lr*wd)                         decoupled weight decay
  *     m  = m*beta1 + g*(1-beta1)
  *     v  = v*beta2 + (g*g)*(1-beta2)
  *     w  = w - (lr/(1-beta1^t)) * (m / (sqrt(v)/sqrt(1-beta2^t) + eps))
  *     working = round-to-nearest-even to the working dtype (NaN -> 0x7FFF)
+ * clip = 1 unless hp->max_grad_norm > 0; then pass 1 also forms the global L2
+ * norm of the unscaled grads g = fp32(grad) * (1/S) in one fixed order (tiles
+ * of 16384 elements per tensor summed in binary32 in a fixed lane/tree order,
+ * tile sums folded in binary64 in a fixed order; the oracle states it), writes
+ * d_state->grad_norm and clip = min(1, max_grad_norm / (norm + 1e-6)) to
+ * d_state->clip_coef ([MPT-ko] "FP16 학습 루프"; [MPT-es] "Operaciones que
+ * permanecen en FP32": gradient norms are long reductions kept in FP32).
+ * Clipping needs d_workspace of mp_adamw_workspace_size(params, n_params)
+ * bytes (device, 4-byte aligned, any contents); without clipping it may be
+ * NULL.
  * The host array `params` (n_params >= 0 entries) is read during the call
  * only; its pointers are device pointers, 16-byte aligned.  grad_dtype and
  * working_dtype are MP_F16 or MP_BF16.  The loss scale itself is not changed
  * here: call loss_scale_update after the step.  Launches at most
- * 2 * ceil(n_params / 512) kernels. */
+ * 2 * ceil(n_params / 512) + 1 kernels. */
+MP_API size_t mp_adamw_workspace_size(const mp_param* params, int32_t n_params);
 MP_API mp_status mp_adamw_step(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
                                mp_dtype working_dtype, const mp_adamw_hparams* hp,
-                               mp_scaler_state* d_state, void* stream);
+                               mp_scaler_state* d_state, void* d_workspace, size_t workspace_bytes,
+                               void* stream);
 
 /* The two passes of mp_adamw_step as separate calls, mirroring the unscale
  * (inf check) and step calls of [MPT-ko] "FP16 학습 루프", so that work such
  * as gradient-norm clipping can run between them.  mp_adamw_check is pass 1
  * (sets found_inf, advances step / beta powers, forms the step scalars from
- * hp); mp_adamw_apply is pass 2 and must follow it on the same stream with the
- * same params and hp.  Each launches ceil(n_params / 512) kernels. */
+ * hp, and the norm and clip coefficient when clipping); mp_adamw_apply is
+ * pass 2 and must follow it on the same stream with the same params and hp.
+ * mp_adamw_check launches ceil(n_params / 512) kernels (+1 with clipping),
+ * mp_adamw_apply ceil(n_params / 512). */
 MP_API mp_status mp_adamw_check(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
-                                const mp_adamw_hparams* hp, mp_scaler_state* d_state, void* stream);
+                                const mp_adamw_hparams* hp, mp_scaler_state* d_state,
+                                void* d_workspace, size_t workspace_bytes, void* stream);
 MP_API mp_status mp_adamw_apply(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
                                 mp_dtype working_dtype, const mp_adamw_hparams* hp,
                                 mp_scaler_state* d_state, void* stream);

@@ -34,7 +34,7 @@ class MpParam(ctypes.Structure):
 
 
 class AdamwHparams(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")]
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")]
 
 
 class ScalerState(ctypes.Structure):
@@ -47,9 +47,11 @@ class ScalerState(ctypes.Structure):
         ("beta1_pow", ctypes.c_double),
         ("beta2_pow", ctypes.c_double),
         ("skipped", ctypes.c_int64),
+        ("grad_norm", ctypes.c_float),
+        ("clip_coef", ctypes.c_float),
         ("internal_found", ctypes.c_uint32),
         ("internal_ticket", ctypes.c_uint32),
-        ("internal_scalars", ctypes.c_float * 8),
+        ("internal_scalars", ctypes.c_float * 6),
     ]
 
 
@@ -93,8 +95,9 @@ def _load() -> ctypes.CDLL:
         "mp_launch_count": (U64, []),
         "mp_scaler_state_init": (None, [P, F]),
         "mp_fp8_meta_init": (None, [P]),
-        "mp_adamw_step": (I32, [P, I32, I32, I32, P, P, P]),
-        "mp_adamw_check": (I32, [P, I32, I32, P, P, P]),
+        "mp_adamw_workspace_size": (S, [P, I32]),
+        "mp_adamw_step": (I32, [P, I32, I32, I32, P, P, P, S, P]),
+        "mp_adamw_check": (I32, [P, I32, I32, P, P, P, S, P]),
         "mp_adamw_apply": (I32, [P, I32, I32, I32, P, P, P]),
         "loss_scale_update": (I32, [P, P, P]),
         "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, P]),
@@ -225,11 +228,25 @@ def make_param_array(params: Sequence[Param]):
     return arr
 
 
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _ptr(workspace), workspace.numel() * workspace.element_size()
+
+
+def mp_adamw_workspace_size(params) -> int:
+    arr = params if isinstance(params, ctypes.Array) else make_param_array(params)
+    return int(lib.mp_adamw_workspace_size(arr, len(params)))
+
+
 def mp_adamw_step(params, hp: AdamwHparams, state, grad_dtype: int | None = None,
-                  working_dtype: int | None = None, stream=None) -> None:
-    """params: a sequence of Param, or a prebuilt ctypes MpParam array (then give dtypes)."""
+                  working_dtype: int | None = None, workspace=None, stream=None) -> None:
+    """params: a sequence of Param, or a prebuilt ctypes MpParam array (then give
+    dtypes).  workspace: device buffer of mp_adamw_workspace_size bytes, needed
+    only when hp.max_grad_norm > 0."""
     arr, n, g, w = _marshal(params, grad_dtype, working_dtype)
-    _check("mp_adamw_step", lib.mp_adamw_step(arr, n, g, w, ctypes.byref(hp), _ptr(state), _stream(stream)))
+    wp, wb = _ws(workspace)
+    _check("mp_adamw_step", lib.mp_adamw_step(arr, n, g, w, ctypes.byref(hp), _ptr(state), wp, wb, _stream(stream)))
 
 
 def _marshal(params, grad_dtype, working_dtype):
@@ -245,9 +262,11 @@ def _marshal(params, grad_dtype, working_dtype):
     return arr, n, grad_dtype, working_dtype
 
 
-def mp_adamw_check(params, hp: AdamwHparams, state, grad_dtype: int | None = None, stream=None) -> None:
+def mp_adamw_check(params, hp: AdamwHparams, state, grad_dtype: int | None = None, workspace=None,
+                   stream=None) -> None:
     arr, n, g, _ = _marshal(params, grad_dtype, MP_F16 if grad_dtype is not None else None)
-    _check("mp_adamw_check", lib.mp_adamw_check(arr, n, g, ctypes.byref(hp), _ptr(state), _stream(stream)))
+    wp, wb = _ws(workspace)
+    _check("mp_adamw_check", lib.mp_adamw_check(arr, n, g, ctypes.byref(hp), _ptr(state), wp, wb, _stream(stream)))
 
 
 def mp_adamw_apply(params, hp: AdamwHparams, state, grad_dtype: int | None = None,
@@ -302,7 +321,8 @@ def rht16(x, y, sign_mask: int, stream=None) -> None:
 __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
-    "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "loss_scale_update", "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
+    "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
+    "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",
     "make_param_array",

@@ -102,6 +102,8 @@ __device__ void finish_check(mp_scaler_state* st, const mp_adamw_hparams hp, boo
   s[S_DECAY] = __double2float_rn(__dsub_rn(1.0, __dmul_rn((double)hp.lr, (double)hp.weight_decay)));
   s[S_OMB1] = __double2float_rn(__dsub_rn(1.0, b1));
   s[S_OMB2] = __double2float_rn(__dsub_rn(1.0, b2));
+  st->grad_norm = -1.0f;  // replaced by k_clip_finish when clipping
+  st->clip_coef = 1.0f;
 }
 
 // A 16-bit word pair has an all-ones exponent (inf/NaN) in a half iff adding
@@ -113,11 +115,24 @@ __device__ __forceinline__ uint32_t nonfinite_bits(uint32_t w) {
   return (w & em) + one;
 }
 
-template <int CAP, bool GBF16>
+template <bool BF16>
+__device__ __forceinline__ float g_lo(uint32_t w) { return BF16 ? bf16lo(w) : f16lo(w); }
+template <bool BF16>
+__device__ __forceinline__ float g_hi(uint32_t w) { return BF16 ? bf16hi(w) : f16hi(w); }
+
+// With CLIP, every tile of kTile elements also yields the binary32 sum of
+// g*g, g = fp32(grad) * inv_scale, in one fixed order: lane t sums its 8
+// vectors (u = 0..7) element by element; each warp folds its 32 lane sums by
+// v[l] += v[l ^ h], h = 16..1; the 8 warp sums fold as w[i] += w[i + h],
+// h = 4, 2, 1.  The sum goes to tile_sums[tile_base + tile].
+template <int CAP, bool GBF16, bool CLIP>
 __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant__ Table<CAP> T,
                                                            mp_scaler_state* st,
-                                                           const mp_adamw_hparams hp, int finalize) {
+                                                           const mp_adamw_hparams hp, int finalize,
+                                                           float* __restrict__ tile_sums, int64_t tile_base) {
+  __shared__ float warp_sum[kThreads / 32];
   uint32_t bad = 0;
+  const float inv_scale = CLIP ? __double2float_rn(__ddiv_rn(1.0, (double)st->scale)) : 0.0f;
   const int64_t total = T.tile_start[T.count];
   for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
     const int ti = find_tensor(T, tile);
@@ -131,15 +146,50 @@ __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant
       full[u] = e + kVec <= d.n;
       if (full[u]) g[u] = ld_cs(d.g + e);
     }
+    float lane = 0.0f;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       if (full[u]) {
         bad |= nonfinite_bits<GBF16>(g[u].x) | nonfinite_bits<GBF16>(g[u].y) |
                nonfinite_bits<GBF16>(g[u].z) | nonfinite_bits<GBF16>(g[u].w);
+        if (CLIP) {
+          const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float a = __fmul_rn(g_lo<GBF16>(gw[k]), inv_scale);
+            lane = __fadd_rn(lane, __fmul_rn(a, a));
+            const float b = __fmul_rn(g_hi<GBF16>(gw[k]), inv_scale);
+            lane = __fadd_rn(lane, __fmul_rn(b, b));
+          }
+        }
       } else {
         const int64_t e = base + ((int64_t)u * kThreads + threadIdx.x) * kVec;
-        for (int64_t i = e; i < d.n; ++i) bad |= nonfinite_bits<GBF16>(d.g[i]) & 0x8000u;
+        for (int64_t i = e; i < d.n; ++i) {
+          const uint32_t h = d.g[i];
+          bad |= nonfinite_bits<GBF16>(h) & 0x8000u;
+          if (CLIP) {
+            const float a = __fmul_rn(g_lo<GBF16>(h), inv_scale);
+            lane = __fadd_rn(lane, __fmul_rn(a, a));
+          }
+        }
       }
+    }
+    if (CLIP) {
+#pragma unroll
+      for (int h = 16; h >= 1; h >>= 1) lane = __fadd_rn(lane, __shfl_xor_sync(0xFFFFFFFFu, lane, h));
+      if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = lane;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float w[kThreads / 32];
+#pragma unroll
+        for (int i = 0; i < kThreads / 32; ++i) w[i] = warp_sum[i];
+#pragma unroll
+        for (int h = kThreads / 64; h >= 1; h >>= 1)
+#pragma unroll
+          for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[i], w[i + h]);
+        tile_sums[tile_base + tile] = w[0];
+      }
+      __syncthreads();  // warp_sum is rewritten by the next tile
     }
   }
   const int any = __syncthreads_or((bad & 0x80008000u) != 0);
@@ -158,13 +208,43 @@ __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant
   }
 }
 
+// Folds the tile sums in binary64 in one fixed order (lane t of 1024 adds
+// tiles t, t + 1024, ...; each warp folds by v[l] += v[l ^ h], h = 16..1; the
+// 32 warp sums fold as w[i] += w[i + h], h = 16..1), then
+// norm = sqrt(total) and clip = min(1, max_norm / (norm + 1e-6)).
+constexpr int kFinishThreads = 1024;
+__global__ __launch_bounds__(kFinishThreads) void k_clip_finish(const float* __restrict__ tile_sums, int64_t ntiles,
+                                                                mp_scaler_state* st, float max_norm) {
+  __shared__ double warp_sum[kFinishThreads / 32];
+  double lane = 0.0;
+  for (int64_t i = threadIdx.x; i < ntiles; i += kFinishThreads) lane = __dadd_rn(lane, (double)tile_sums[i]);
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) lane = __dadd_rn(lane, __shfl_xor_sync(0xFFFFFFFFu, lane, h));
+  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = lane;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double w[kFinishThreads / 32];
+#pragma unroll
+    for (int i = 0; i < kFinishThreads / 32; ++i) w[i] = warp_sum[i];
+#pragma unroll
+    for (int h = kFinishThreads / 64; h >= 1; h >>= 1)
+#pragma unroll
+      for (int i = 0; i < h; ++i) w[i] = __dadd_rn(w[i], w[i + h]);
+    const double norm = __dsqrt_rn(w[0]);
+    double c = __ddiv_rn((double)max_norm, __dadd_rn(norm, 1e-6));
+    if (c > 1.0) c = 1.0;
+    st->grad_norm = __double2float_rn(norm);
+    st->clip_coef = __double2float_rn(c);
+  }
+}
+
 struct Scalars {
-  float inv_scale, step_size, bc2s, decay, omb1, omb2, beta1, beta2, eps;
+  float inv_scale, step_size, bc2s, decay, omb1, omb2, beta1, beta2, eps, clip;
 };
 
 // One element, binary32, in the order of the documented update.
 __device__ __forceinline__ void adamw_elem(float graw, float& w, float& m, float& v, const Scalars& s) {
-  const float g = __fmul_rn(graw, s.inv_scale);
+  const float g = __fmul_rn(__fmul_rn(graw, s.inv_scale), s.clip);  // unscale, then clip
   const float wd = __fmul_rn(w, s.decay);
   m = __fadd_rn(__fmul_rn(m, s.beta1), __fmul_rn(g, s.omb1));
   v = __fadd_rn(__fmul_rn(v, s.beta2), __fmul_rn(__fmul_rn(g, g), s.omb2));
@@ -172,10 +252,6 @@ __device__ __forceinline__ void adamw_elem(float graw, float& w, float& m, float
   w = __fsub_rn(wd, __fmul_rn(s.step_size, __fdiv_rn(m, den)));
 }
 
-template <bool BF16>
-__device__ __forceinline__ float g_lo(uint32_t w) { return BF16 ? bf16lo(w) : f16lo(w); }
-template <bool BF16>
-__device__ __forceinline__ float g_hi(uint32_t w) { return BF16 ? bf16hi(w) : f16hi(w); }
 template <bool BF16>
 __device__ __forceinline__ uint32_t pack16(float lo, float hi) {
   return BF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
@@ -267,7 +343,8 @@ __global__ __launch_bounds__(kUpdateThreads) void k_adamw_update(const __grid_co
   s.beta1 = beta1;
   s.beta2 = beta2;
   s.eps = eps;
-  const int t = threadIdx.x;  // 0 .. 255
+  s.clip = st->clip_coef;
+  const int t = threadIdx.x;
   int it = 0;
   for (int64_t c = blockIdx.x; c < total; c += gridDim.x, ++it) {
     const int sidx = it % kStages;
@@ -340,15 +417,29 @@ void fill_table(Table<CAP>& T, const mp_param* const* list, int count, int64_t t
   T.tile_start[count] = acc;
 }
 
+struct ClipArgs {
+  bool on;
+  float* tile_sums;
+  float max_norm;
+};
+
 template <int CAP, bool GBF16, bool WBF16>
 mp_status launch_group(const mp_param* const* list, int count, bool finalize, bool update,
-                       const mp_adamw_hparams& hp, mp_scaler_state* st, cudaStream_t s) {
+                       const mp_adamw_hparams& hp, mp_scaler_state* st, const ClipArgs& clip, int64_t tile_base,
+                       int64_t* tiles_out, cudaStream_t s) {
   Table<CAP> Tl;  // copied by value into the launch's parameter buffer
   if (!update) {
     fill_table(Tl, list, count, kTile);
-    static const int occ = occupancy(k_check_finite<CAP, GBF16>, kThreads, 0);
-    k_check_finite<CAP, GBF16><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(Tl, st, hp,
-                                                                                         finalize ? 1 : 0);
+    *tiles_out = Tl.tile_start[count];
+    if (clip.on) {
+      static const int occ = occupancy(k_check_finite<CAP, GBF16, true>, kThreads, 0);
+      k_check_finite<CAP, GBF16, true><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(
+          Tl, st, hp, finalize ? 1 : 0, clip.tile_sums, tile_base);
+    } else {
+      static const int occ = occupancy(k_check_finite<CAP, GBF16, false>, kThreads, 0);
+      k_check_finite<CAP, GBF16, false><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(
+          Tl, st, hp, finalize ? 1 : 0, nullptr, 0);
+    }
   } else {
     fill_table(Tl, list, count, kChunk);
     static const int occ = [] {
@@ -363,31 +454,49 @@ mp_status launch_group(const mp_param* const* list, int count, bool finalize, bo
   return launch_status();
 }
 
-// pass 0: check (only the last group finalises); pass 1: update.
+// pass 0: check (only the last group finalises; then the norm when clipping);
+// pass 1: update.
 template <bool GBF16, bool WBF16>
 mp_status run_pass(int pass, const mp_param* const* list, int n, const mp_adamw_hparams& hp, mp_scaler_state* st,
-                   cudaStream_t s) {
+                   const ClipArgs& clip, cudaStream_t s) {
   int first = 0;
+  int64_t tile_base = 0;
   do {
     const int count = (n - first) < kBigCap ? (n - first) : kBigCap;
     const bool last = first + count >= n;
+    int64_t tiles = 0;
     const mp_status rc =
         (count <= kSmallCap)
-            ? launch_group<kSmallCap, GBF16, WBF16>(list + first, count, last, pass == 1, hp, st, s)
-            : launch_group<kBigCap, GBF16, WBF16>(list + first, count, last, pass == 1, hp, st, s);
+            ? launch_group<kSmallCap, GBF16, WBF16>(list + first, count, last, pass == 1, hp, st, clip, tile_base,
+                                                    &tiles, s)
+            : launch_group<kBigCap, GBF16, WBF16>(list + first, count, last, pass == 1, hp, st, clip, tile_base,
+                                                  &tiles, s);
     if (rc != MP_OK) return rc;
+    tile_base += tiles;
     first += count;
   } while (first < n);
+  if (pass == 0 && clip.on) {
+    k_clip_finish<<<1, kFinishThreads, 0, s>>>(clip.tile_sums, tile_base, st, clip.max_norm);
+    note_launches(1);
+    return launch_status();
+  }
   return MP_OK;
 }
 
 mp_status dispatch_pass(int pass, const mp_param* const* list, int n, mp_dtype gdt, mp_dtype wdt,
-                        const mp_adamw_hparams& hp, mp_scaler_state* st, cudaStream_t s) {
+                        const mp_adamw_hparams& hp, mp_scaler_state* st, const ClipArgs& clip, cudaStream_t s) {
   const bool gb = gdt == MP_BF16, wb = wdt == MP_BF16;
-  if (!gb && !wb) return run_pass<false, false>(pass, list, n, hp, st, s);
-  if (!gb && wb) return run_pass<false, true>(pass, list, n, hp, st, s);
-  if (gb && !wb) return run_pass<true, false>(pass, list, n, hp, st, s);
-  return run_pass<true, true>(pass, list, n, hp, st, s);
+  if (!gb && !wb) return run_pass<false, false>(pass, list, n, hp, st, clip, s);
+  if (!gb && wb) return run_pass<false, true>(pass, list, n, hp, st, clip, s);
+  if (gb && !wb) return run_pass<true, false>(pass, list, n, hp, st, clip, s);
+  return run_pass<true, true>(pass, list, n, hp, st, clip, s);
+}
+
+int64_t clip_tiles(const mp_param* params, int32_t n_params) {
+  int64_t t = 0;
+  for (int i = 0; i < n_params; ++i)
+    if (params[i].numel > 0) t += (params[i].numel + kTile - 1) / kTile;
+  return t;
 }
 
 bool finite_f(float x) { return x == x && x - x == 0.0f; }
@@ -406,14 +515,21 @@ namespace {
 // in `passes` (bit 0: check, bit 1: update).
 mp_status adamw_entry(int passes, const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
                       mp_dtype working_dtype, const mp_adamw_hparams* hp, mp_scaler_state* d_state,
-                      void* stream) {
+                      void* d_workspace, size_t workspace_bytes, void* stream) {
   if (n_params < 0 || (n_params > 0 && !params) || !hp || !d_state) return MP_EINVAL;
   if ((reinterpret_cast<uintptr_t>(d_state) & 7u) != 0) return MP_EALIGN;
   if ((grad_dtype != MP_F16 && grad_dtype != MP_BF16) || (working_dtype != MP_F16 && working_dtype != MP_BF16))
     return MP_EINVAL;
   if (!finite_f(hp->lr) || !finite_f(hp->weight_decay) || !finite_f(hp->eps) || hp->eps < 0.0f ||
-      !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f))
+      !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) ||
+      !finite_f(hp->max_grad_norm) || hp->max_grad_norm < 0.0f)
     return MP_EINVAL;
+  ClipArgs clip{(passes & 1) && hp->max_grad_norm > 0.0f, static_cast<float*>(d_workspace), hp->max_grad_norm};
+  if (clip.on) {
+    if (!d_workspace || workspace_bytes < (size_t)clip_tiles(params, n_params) * sizeof(float))
+      return MP_EWORKSPACE;
+    if (reinterpret_cast<uintptr_t>(d_workspace) & 3u) return MP_EALIGN;
+  }
   const mp_param* small[64];
   const mp_param** heap = nullptr;
   const mp_param** list = small;
@@ -435,8 +551,8 @@ mp_status adamw_entry(int passes, const mp_param* params, int32_t n_params, mp_d
     else list[n++] = &p;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (rc == MP_OK && (passes & 1)) rc = dispatch_pass(0, list, n, grad_dtype, working_dtype, *hp, d_state, s);
-  if (rc == MP_OK && (passes & 2)) rc = dispatch_pass(1, list, n, grad_dtype, working_dtype, *hp, d_state, s);
+  if (rc == MP_OK && (passes & 1)) rc = dispatch_pass(0, list, n, grad_dtype, working_dtype, *hp, d_state, clip, s);
+  if (rc == MP_OK && (passes & 2)) rc = dispatch_pass(1, list, n, grad_dtype, working_dtype, *hp, d_state, clip, s);
   delete[] heap;
   return rc;
 }
@@ -446,21 +562,30 @@ mp_status adamw_entry(int passes, const mp_param* params, int32_t n_params, mp_d
 
 extern "C" {
 
+MP_API size_t mp_adamw_workspace_size(const mp_param* params, int32_t n_params) {
+  if (!params || n_params <= 0) return 0;
+  return (size_t)mp::clip_tiles(params, n_params) * sizeof(float);
+}
+
 MP_API mp_status mp_adamw_step(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
                                mp_dtype working_dtype, const mp_adamw_hparams* hp,
-                               mp_scaler_state* d_state, void* stream) {
-  return mp::adamw_entry(3, params, n_params, grad_dtype, working_dtype, hp, d_state, stream);
+                               mp_scaler_state* d_state, void* d_workspace, size_t workspace_bytes,
+                               void* stream) {
+  return mp::adamw_entry(3, params, n_params, grad_dtype, working_dtype, hp, d_state, d_workspace,
+                         workspace_bytes, stream);
 }
 
 MP_API mp_status mp_adamw_check(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
-                                const mp_adamw_hparams* hp, mp_scaler_state* d_state, void* stream) {
-  return mp::adamw_entry(1, params, n_params, grad_dtype, MP_F16, hp, d_state, stream);
+                                const mp_adamw_hparams* hp, mp_scaler_state* d_state, void* d_workspace,
+                                size_t workspace_bytes, void* stream) {
+  return mp::adamw_entry(1, params, n_params, grad_dtype, MP_F16, hp, d_state, d_workspace, workspace_bytes,
+                         stream);
 }
 
 MP_API mp_status mp_adamw_apply(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,
                                 mp_dtype working_dtype, const mp_adamw_hparams* hp,
                                 mp_scaler_state* d_state, void* stream) {
-  return mp::adamw_entry(2, params, n_params, grad_dtype, working_dtype, hp, d_state, stream);
+  return mp::adamw_entry(2, params, n_params, grad_dtype, working_dtype, hp, d_state, nullptr, 0, stream);
 }
 
 MP_API mp_status loss_scale_update(mp_scaler_state* d_state, const mp_scaler_cfg* cfg, void* stream) {

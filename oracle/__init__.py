@@ -33,7 +33,7 @@ def build(force: bool = False) -> str:
 
 
 class AdamwHp(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay")]
+    _fields_ = [(n, ctypes.c_float) for n in ("lr", "beta1", "beta2", "eps", "weight_decay", "max_grad_norm")]
 
 
 class ScalerState(ctypes.Structure):
@@ -61,7 +61,7 @@ class ScalerCfg(ctypes.Structure):
 class StepScalars(ctypes.Structure):
     _fields_ = [
         (n, ctypes.c_float)
-        for n in ("inv_scale", "step_size", "bc2_sqrt", "decay", "omb1", "omb2", "beta1", "beta2", "eps")
+        for n in ("inv_scale", "step_size", "bc2_sqrt", "decay", "omb1", "omb2", "beta1", "beta2", "eps", "clip")
     ]
 
 
@@ -112,6 +112,9 @@ def lib() -> ctypes.CDLL:
             "orc_adamw_begin": (None, [P, P, ctypes.c_int, P]),
             "orc_adamw_apply": (None, [P, P, P, P, P, ctypes.c_int, P, ctypes.c_int, I64]),
             "orc_loss_scale_update": (None, [P, P]),
+            "orc_grad_tile_sums": (None, [P, ctypes.c_int, I64, F, P]),
+            "orc_sum_tile_sums": (ctypes.c_double, [P, I64]),
+            "orc_clip_coef": (F, [ctypes.c_double, F]),
             "orc_fp8_cast_one": (U8, [F, F, ctypes.c_int]),
             "orc_fp8_cast_array": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, F]),
             "orc_fp8_history_update": (None, [P, P, I32, F, F, ctypes.c_int]),
@@ -339,18 +342,50 @@ def nvfp4_block_scale(bamax: float, s_t: float):
     return int(c[0]), float(d[0]), float(r[0])
 
 
-def adamw_step(hp: AdamwHp, st: ScalerState, tensors, g_fmt: int, w16_fmt: int) -> int:
+CLIP_TILE = 16384
+
+
+def grad_tile_sums(g: np.ndarray, g_fmt: int, inv_scale: float) -> np.ndarray:
+    g = np.ascontiguousarray(g, dtype=np.uint16)
+    out = np.zeros((g.size + CLIP_TILE - 1) // CLIP_TILE, dtype=np.float32)
+    lib().orc_grad_tile_sums(_p(g), g_fmt, g.size, np.float32(inv_scale), _p(out))
+    return out
+
+
+def sum_tile_sums(tiles: np.ndarray) -> float:
+    tiles = np.ascontiguousarray(tiles, dtype=np.float32)
+    return float(lib().orc_sum_tile_sums(_p(tiles), tiles.size))
+
+
+def clip_coef(norm: float, max_norm: float) -> float:
+    return float(np.float32(lib().orc_clip_coef(float(norm), np.float32(max_norm))))
+
+
+def grad_norm(grads, g_fmt: int, inv_scale: float) -> float:
+    """Global L2 norm of the unscaled grads, in the fixed order of oracle.h."""
+    tiles = [grad_tile_sums(g, g_fmt, inv_scale) for g in grads if g.size]
+    total = sum_tile_sums(np.concatenate(tiles) if tiles else np.zeros(0, np.float32))
+    return float(np.sqrt(total))
+
+
+def adamw_step(hp: AdamwHp, st: ScalerState, tensors, g_fmt: int, w16_fmt: int):
     """One optimizer step over a list of (w, m, v, g, w16) numpy tensors.
 
     found_inf is the OR over every grad of the step; when set the step is
-    skipped and nothing is written.  Returns found_inf."""
+    skipped and nothing is written.  With hp.max_grad_norm > 0 the unscaled
+    grads are clipped to that global norm.  Returns (found_inf, grad norm or
+    None, clip coefficient)."""
     found = 0
     for (_, _, _, g, _) in tensors:
         if nonfinite_any(g, g_fmt):
             found = 1
             break
     s = adamw_begin(hp, st, found)
+    norm = None
+    if hp.max_grad_norm > 0:
+        norm = grad_norm([g for (_, _, _, g, _) in tensors], g_fmt, s.inv_scale)
+        s.clip = clip_coef(norm, hp.max_grad_norm)
     if not found:
         for (w, m, v, g, w16) in tensors:
             adamw_apply(s, w, m, v, g, g_fmt, w16, w16_fmt)
-    return found
+    return found, norm, s.clip

@@ -321,13 +321,14 @@ void orc_adamw_begin(const orc_adamw_hp* hp, orc_scaler_state* st, int found_inf
   out->beta1 = hp->beta1;
   out->beta2 = hp->beta2;
   out->eps = hp->eps;
+  out->clip = 1.0f;
 }
 
 void orc_adamw_apply(const orc_step_scalars* s, float* w, float* m, float* v, const uint16_t* g,
                      int g_fmt, uint16_t* w16, int w16_fmt, int64_t n) {
   for (int64_t i = 0; i < n; ++i) {
     float gf = (g_fmt == ORC_F16) ? orc_f16_to_f32(g[i]) : orc_bf16_to_f32(g[i]);
-    float gu = gf * s->inv_scale;                    /* unscale */
+    float gu = (gf * s->inv_scale) * s->clip;       /* unscale, then clip */
     float wi = w[i] * s->decay;                      /* decoupled decay */
     float mi = m[i] * s->beta1 + gu * s->omb1;       /* first moment */
     float vi = v[i] * s->beta2 + (gu * gu) * s->omb2; /* second moment */
@@ -338,6 +339,67 @@ void orc_adamw_apply(const orc_step_scalars* s, float* w, float* m, float* v, co
     v[i] = vi;
     w16[i] = (w16_fmt == ORC_F16) ? orc_f32_to_f16(wi) : orc_f32_to_bf16(wi);
   }
+}
+
+/* Global gradient norm in the fixed order stated in oracle.h. */
+void orc_grad_tile_sums(const uint16_t* g, int g_fmt, int64_t n, float inv_scale, float* tile_sums) {
+  int64_t ntiles = (n + ORC_CLIP_TILE - 1) / ORC_CLIP_TILE;
+  float lane[256], grp[8];
+  for (int64_t tile = 0; tile < ntiles; ++tile) {
+    int64_t base = tile * ORC_CLIP_TILE;
+    for (int t = 0; t < 256; ++t) {
+      float s = 0.0f;
+      for (int u = 0; u < 8; ++u)
+        for (int k = 0; k < 8; ++k) {
+          int64_t i = base + u * 2048 + t * 8 + k;
+          if (i >= n) continue;
+          float gf = (g_fmt == ORC_F16) ? orc_f16_to_f32(g[i]) : orc_bf16_to_f32(g[i]);
+          float gu = gf * inv_scale;
+          s = s + gu * gu;
+        }
+      lane[t] = s;
+    }
+    for (int w = 0; w < 8; ++w) {
+      float v[32], nv[32];
+      for (int l = 0; l < 32; ++l) v[l] = lane[w * 32 + l];
+      for (int h = 16; h >= 1; h >>= 1) {
+        for (int l = 0; l < 32; ++l) nv[l] = v[l] + v[l ^ h];
+        for (int l = 0; l < 32; ++l) v[l] = nv[l];
+      }
+      grp[w] = v[0];
+    }
+    for (int h = 4; h >= 1; h >>= 1)
+      for (int i = 0; i < h; ++i) grp[i] = grp[i] + grp[i + h];
+    tile_sums[tile] = grp[0];
+  }
+}
+
+double orc_sum_tile_sums(const float* tile_sums, int64_t ntiles) {
+  double lane[1024];
+  double grp[32];
+  for (int t = 0; t < 1024; ++t) {
+    double s = 0.0;
+    for (int64_t i = t; i < ntiles; i += 1024) s = s + (double)tile_sums[i];
+    lane[t] = s;
+  }
+  for (int w = 0; w < 32; ++w) {
+    double v[32], nv[32];
+    for (int l = 0; l < 32; ++l) v[l] = lane[w * 32 + l];
+    for (int h = 16; h >= 1; h >>= 1) {
+      for (int l = 0; l < 32; ++l) nv[l] = v[l] + v[l ^ h];
+      for (int l = 0; l < 32; ++l) v[l] = nv[l];
+    }
+    grp[w] = v[0];
+  }
+  for (int h = 16; h >= 1; h >>= 1)
+    for (int i = 0; i < h; ++i) grp[i] = grp[i] + grp[i + h];
+  return grp[0];
+}
+
+float orc_clip_coef(double norm, float max_norm) {
+  double c = (double)max_norm / (norm + 1e-6);
+  if (c > 1.0) c = 1.0;
+  return (float)c;
 }
 
 /* [MPT-ko] "손실 스케일링": start large, on inf/NaN skip and shrink (x0.5),

@@ -78,6 +78,7 @@ int orc_rht16(const uint16_t* x_bf16, int64_t rows, int64_t cols, uint16_t sign_
 /* ---- mixed-precision optimizer step ----------------------------------------- */
 typedef struct {
   float lr, beta1, beta2, eps, weight_decay;
+  float max_grad_norm; /* > 0: clip the unscaled grads to this global L2 norm */
 } orc_adamw_hp;
 
 typedef struct {
@@ -96,9 +97,9 @@ typedef struct {
   int32_t growth_interval, enabled;
 } orc_scaler_cfg;
 
-/* Per-step scalars, rounded once from binary64. */
+/* Per-step scalars, rounded once from binary64; clip = 1 without clipping. */
 typedef struct {
-  float inv_scale, step_size, bc2_sqrt, decay, omb1, omb2, beta1, beta2, eps;
+  float inv_scale, step_size, bc2_sqrt, decay, omb1, omb2, beta1, beta2, eps, clip;
 } orc_step_scalars;
 
 /* 1 if any of the n 16-bit grads (fmt ORC_F16 / ORC_BF16) is inf or NaN. */
@@ -109,6 +110,26 @@ void orc_adamw_begin(const orc_adamw_hp* hp, orc_scaler_state* st, int found_inf
 /* Unscale + AdamW on the FP32 master + rounded 16-bit copy, element-wise. */
 void orc_adamw_apply(const orc_step_scalars* s, float* w, float* m, float* v, const uint16_t* g,
                      int g_fmt, uint16_t* w16, int w16_fmt, int64_t n);
+/* Gradient-norm clipping ([MPT-ko] "FP16 학습 루프": clip_grad_norm_(max_norm=1.0)
+ * after unscale_; [MPT-es] "Operaciones que permanecen en FP32": long
+ * reductions such as gradient norms stay in FP32).  The sum of squares of
+ * the unscaled grads g = fp32(grad) * inv_scale uses one fixed order:
+ *   tiles of 16384 elements per tensor (the last one short);
+ *   in a tile, lane t (0..255) sums, in binary32, g*g of the elements
+ *     u*2048 + t*8 + k for u = 0..7, then k = 0..7;
+ *   the 256 lane sums fold as 8 groups of 32: in each, v[l] += v[l ^ h] for
+ *     h = 16, 8, 4, 2, 1, keeping v[0]; the 8 group results w fold as
+ *     w[i] += w[i + h] for i < h, h = 4, 2, 1, keeping w[0];
+ *   tile sums, in tile order over all tensors, fold in binary64: lane t of
+ *     1024 adds tiles t, t + 1024, ... in order, then the 1024 lane sums fold
+ *     as 32 groups of 32 (v[l] += v[l ^ h], h = 16..1) and the 32 group
+ *     results as w[i] += w[i + h], h = 16..1.
+ * norm = sqrt(total); clip = min(1, max_norm / (norm + 1e-6)), binary64,
+ * rounded to binary32. */
+#define ORC_CLIP_TILE 16384
+void orc_grad_tile_sums(const uint16_t* g, int g_fmt, int64_t n, float inv_scale, float* tile_sums);
+double orc_sum_tile_sums(const float* tile_sums, int64_t ntiles);
+float orc_clip_coef(double norm, float max_norm);
 /* Dynamic loss-scale update from st->found_inf. */
 void orc_loss_scale_update(orc_scaler_state* st, const orc_scaler_cfg* cfg);
 

@@ -259,3 +259,157 @@ def test_check_then_apply_equals_fused_step():
     for x, y in ((A.w, B.w), (A.m, B.m), (A.v, B.v), (A.w16, B.w16)):
         assert torch.equal(x.view(torch.int8) if x.dtype != torch.float32 else x, y.view(torch.int8) if y.dtype != torch.float32 else y)
     assert bytes(M.read_scaler_state(sa)) == bytes(M.read_scaler_state(sb))
+
+
+# ---- gradient-norm clipping fused into the check pass -----------------------------
+
+
+def assert_norm_equal(g_norm, g_coef, o_norm, o_coef, what=""):
+    gn, on = np.float32(g_norm), np.float32(o_norm)
+    if np.isfinite(on):
+        assert gn.view(np.uint32) == on.view(np.uint32), f"{what} norm {gn} vs {on}"
+        assert np.float32(g_coef).view(np.uint32) == np.float32(o_coef).view(np.uint32), f"{what} clip"
+    else:
+        assert not np.isfinite(gn) and np.isnan(gn) == np.isnan(on), f"{what} norm {gn} vs {on}"
+
+
+def test_tiny_step_with_clipping():
+    c = W.TINY
+    t = golden("scaler_trajectory_tiny.json")
+    max_norm = 0.05  # the unscaled grads have a norm near 0.1: clipping is active
+    ghp = M.AdamwHparams(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, max_norm)
+    ohp = O.AdamwHp(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, max_norm)
+    cfg, ocfg = M.ScalerCfg(c.growth, c.backoff, c.interval, 1), O.ScalerCfg(c.growth, c.backoff, c.interval, 1)
+    T = Tensors(synth.fill(c.master_recipe(), synth.F32, c.n), O.F16, O.F16)
+    ws = torch.empty(M.mp_adamw_workspace_size([T.param()]), dtype=torch.uint8, device="cuda")
+    st, ost = M.new_scaler_state(c.init_scale), O.new_scaler_state(c.init_scale)
+    clipped = 0
+    for k in range(1, c.steps + 1):
+        g = synth.fill(c.grad_recipe(k, t["scale_used"][k - 1]), synth.F16, c.n)
+        inj = c.injection(k)
+        if inj:
+            g[inj[0]] = inj[1]
+        T.g.copy_(to_dev(g, torch.float16))
+        M.mp_adamw_step([T.param()], ghp, st, workspace=ws)
+        M.loss_scale_update(st, cfg)
+        found, norm, coef = O.adamw_step(ohp, ost, [T.oracle_tuple(g)], O.F16, O.F16)
+        O.loss_scale_update(ost, ocfg)
+        torch.cuda.synchronize()
+        gs = M.read_scaler_state(st)
+        assert_state_equal(gs, ost)
+        assert_norm_equal(gs.grad_norm, gs.clip_coef, norm, coef, f"step {k}")
+        clipped += int(coef < 1.0)
+        T.compare(f"step {k}")
+    assert clipped >= 8
+
+
+@pytest.mark.parametrize("g_fmt", [O.F16, O.BF16])
+def test_ragged_multi_tensor_with_clipping(g_fmt):
+    sizes = [1, 7, 16383, 16384, 16385, 40000, 0, 100_003]
+    ghp = M.AdamwHparams(3e-3, 0.8, 0.99, 1e-6, 0.1, 0.5)
+    ohp = O.AdamwHp(3e-3, 0.8, 0.99, 1e-6, 0.1, 0.5)
+    S0 = 256.0 if g_fmt == O.F16 else 1.0
+    Ts = [Tensors(synth.fill(synth.recipe(50, i, 0.5), synth.F32, n), g_fmt, O.BF16) for i, n in enumerate(sizes)]
+    ws = torch.empty(M.mp_adamw_workspace_size([T.param() for T in Ts]), dtype=torch.uint8, device="cuda")
+    st, ost = M.new_scaler_state(S0), O.new_scaler_state(S0)
+    for k in range(1, 4):
+        hosts = []
+        for i, (T, n) in enumerate(zip(Ts, sizes)):
+            g = synth.fill(synth.recipe(51, 100 * k + i, float(np.float32(0.01 * S0))),
+                           synth.F16 if g_fmt == O.F16 else synth.BF16, n)
+            hosts.append(g)
+            if n:
+                T.g.copy_(to_dev(g, TD[g_fmt]))
+        M.mp_adamw_step([T.param() for T in Ts], ghp, st, workspace=ws)
+        found, norm, coef = O.adamw_step(ohp, ost, [T.oracle_tuple(g) for T, g in zip(Ts, hosts)], g_fmt, O.BF16)
+        torch.cuda.synchronize()
+        gs = M.read_scaler_state(st)
+        assert_state_equal(gs, ost)
+        assert_norm_equal(gs.grad_norm, gs.clip_coef, norm, coef, f"step {k}")
+        assert coef < 1.0
+        for i, T in enumerate(Ts):
+            T.compare(f"step {k} tensor {i}")
+
+
+def test_clipping_across_launch_groups():
+    rng = np.random.default_rng(4)
+    sizes = rng.integers(1, 20000, size=600).tolist()
+    ghp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0)
+    ohp = O.AdamwHp(1e-3, 0.9, 0.999, 1e-8, 0.01, 1.0)
+    Ts = [Tensors(synth.fill(synth.recipe(60, i, 0.02), synth.F32, n), O.BF16, O.BF16) for i, n in enumerate(sizes)]
+    ws = torch.empty(M.mp_adamw_workspace_size([T.param() for T in Ts]), dtype=torch.uint8, device="cuda")
+    st, ost = M.new_scaler_state(1.0), O.new_scaler_state(1.0)
+    hosts = []
+    for i, (T, n) in enumerate(zip(Ts, sizes)):
+        g = synth.fill(synth.recipe(61, i, 1e-3), synth.BF16, n)
+        hosts.append(g)
+        T.g.copy_(to_dev(g, torch.bfloat16))
+    M.mp_adamw_check([T.param() for T in Ts], ghp, st, workspace=ws)
+    M.mp_adamw_apply([T.param() for T in Ts], ghp, st)
+    found, norm, coef = O.adamw_step(ohp, ost, [T.oracle_tuple(g) for T, g in zip(Ts, hosts)], O.BF16, O.BF16)
+    torch.cuda.synchronize()
+    gs = M.read_scaler_state(st)
+    assert_norm_equal(gs.grad_norm, gs.clip_coef, norm, coef)
+    for i in (0, 511, 512, 599):
+        Ts[i].compare(f"tensor {i}")
+
+
+def test_full_model_clipping_norm_and_sampled_update():
+    """Llama-3-8B list, 2 steps with max_grad_norm 1.0: the norm over all
+    8.03e9 grads against the oracle (tile sums per tensor in parallel on the
+    host, from the generator's grads copied back), then sampled elements."""
+    import concurrent.futures as cf
+
+    c = W.FULL
+    params = W.llama3_8b_params()
+    total = sum(n for _, n in params)
+    free, _ = torch.cuda.mem_get_info()
+    if free < total * 16 + (8 << 30):
+        pytest.skip("not enough device memory for the full model")
+    max_norm = 1.0
+    ghp = M.AdamwHparams(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, max_norm)
+    ohp = O.AdamwHp(c.lr, c.beta1, c.beta2, c.eps, c.weight_decay, max_norm)
+    ws_, ms, vs, gs, w16s = [], [], [], [], []
+    for t, (name, n) in enumerate(params):
+        w = torch.empty(n, dtype=torch.float32, device="cuda")
+        synth.fill_device(c.master_recipe(t), synth.F32, w)
+        ws_.append(w)
+        ms.append(torch.zeros(n, dtype=torch.float32, device="cuda"))
+        vs.append(torch.zeros(n, dtype=torch.float32, device="cuda"))
+        gs.append(torch.empty(n, dtype=torch.float16, device="cuda"))
+        w16s.append(torch.empty(n, dtype=torch.bfloat16, device="cuda"))
+    plist = [M.Param(ws_[i], ms[i], vs[i], gs[i], w16s[i]) for i in range(len(params))]
+    work = torch.empty(M.mp_adamw_workspace_size(plist), dtype=torch.uint8, device="cuda")
+    rng = np.random.default_rng(8)
+    samples = [np.unique(rng.integers(0, n, 64)).astype(np.int64) for _, n in params]
+    ow = [synth.fill_at(c.master_recipe(t), synth.F32, idx) for t, idx in enumerate(samples)]
+    om = [np.zeros(i.size, np.float32) for i in samples]
+    ov = [np.zeros(i.size, np.float32) for i in samples]
+    ow16 = [np.zeros(i.size, np.uint16) for i in samples]
+    st, ost = M.new_scaler_state(c.scale), O.new_scaler_state(c.scale)
+    for step in (1, 2):
+        for t in range(len(params)):
+            synth.fill_device(c.grad_recipe(t, step), synth.F16, gs[t])
+        M.mp_adamw_step(plist, ghp, st, workspace=work)
+        s_orc = O.adamw_begin(ohp, ost, 0)
+        inv = s_orc.inv_scale
+
+        def tiles(t):
+            return O.grad_tile_sums(to_host(gs[t], np.uint16), O.F16, inv)
+
+        with cf.ThreadPoolExecutor(16) as ex:
+            parts = list(ex.map(tiles, range(len(params))))
+        norm = float(np.sqrt(O.sum_tile_sums(np.concatenate(parts))))
+        s_orc.clip = O.clip_coef(norm, max_norm)
+        for t, idx in enumerate(samples):
+            O.adamw_apply(s_orc, ow[t], om[t], ov[t], synth.fill_at(c.grad_recipe(t, step), synth.F16, idx), O.F16,
+                          ow16[t], O.BF16)
+        torch.cuda.synchronize()
+        gst = M.read_scaler_state(st)
+        assert_norm_equal(gst.grad_norm, gst.clip_coef, norm, s_orc.clip, f"step {step}")
+        assert gst.clip_coef < 1.0
+    for t, idx in enumerate(samples):
+        it = torch.from_numpy(idx).cuda()
+        for gt, ot in ((ws_[t], ow[t]), (ms[t], om[t]), (vs[t], ov[t])):
+            assert ulp_diff(gt[it].cpu().numpy(), ot).max() == 0, params[t][0]
+        np.testing.assert_array_equal(to_host(w16s[t][it], np.uint16), ow16[t])

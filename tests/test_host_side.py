@@ -43,7 +43,7 @@ def test_struct_layouts(M):
     st = M.ScalerState()
     M.lib.mp_scaler_state_init(ctypes.byref(st), 65536.0)
     assert st.scale == 65536.0 and st.beta1_pow == 1.0 and st.beta2_pow == 1.0 and st.step == 0
-    assert ctypes.sizeof(M.ScalerState) == 88 and M.ScalerState.internal_found.offset == 48
+    assert ctypes.sizeof(M.ScalerState) == 88 and M.ScalerState.internal_found.offset == 56
     m = M.Fp8Meta()
     M.lib.mp_fp8_meta_init(ctypes.byref(m))
     assert (m.scale, m.scale_inv, m.amax, m.pos) == (1.0, 1.0, 0.0, 0)
@@ -55,13 +55,21 @@ def test_struct_layouts(M):
 def test_argument_validation_without_gpu(M):
     L = M.lib
     hp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
-    assert L.mp_adamw_step(None, 0, 9, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EINVAL
-    assert L.mp_adamw_step(None, -1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EINVAL
-    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(hp), 12, None) == M.MP_EALIGN
+    assert L.mp_adamw_step(None, 0, 9, M.MP_F16, ctypes.byref(hp), 16, None, 0, None) == M.MP_EINVAL
+    assert L.mp_adamw_step(None, -1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None, 0, None) == M.MP_EINVAL
+    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(hp), 12, None, 0, None) == M.MP_EALIGN
     bad = M.AdamwHparams(float("nan"), 0.9, 0.999, 1e-8, 0.0)
-    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(bad), 16, None) == M.MP_EINVAL
+    assert L.mp_adamw_step(None, 0, M.MP_F16, M.MP_F16, ctypes.byref(bad), 16, None, 0, None) == M.MP_EINVAL
     p = (M.MpParam * 1)(M.MpParam(16, 16, 16, 24, 16, 5))
-    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None) == M.MP_EALIGN
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None, 0, None) == M.MP_EALIGN
+    # clipping needs a workspace of mp_adamw_workspace_size bytes
+    clip = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0)
+    p = (M.MpParam * 1)(M.MpParam(16, 16, 16, 16, 16, 40000))
+    assert L.mp_adamw_workspace_size(p, 1) == 4 * 3
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, None, 0, None) == M.MP_EWORKSPACE
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, 18, 12, None) == M.MP_EALIGN
+    neg = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, -1.0)
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(neg), 16, None, 0, None) == M.MP_EINVAL
     cfg = M.ScalerCfg(2.0, 0.5, 0, 1)
     assert L.loss_scale_update(16, ctypes.byref(cfg), None) == M.MP_EINVAL
     assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_F16, 16, 16, 4, 1.0, None) == M.MP_EINVAL

@@ -137,7 +137,7 @@ def test_skipped_step_writes_nothing():
     w16 = np.full(4, 7, np.uint16)
     g = O.convert(np.array([1, 2, np.inf, 3], np.float32), O.F32, O.F16)
     st = O.new_scaler_state()
-    found = O.adamw_step(hp(), st, [(w, m, v, g, w16)], O.F16, O.F16)
+    found, _, _ = O.adamw_step(hp(), st, [(w, m, v, g, w16)], O.F16, O.F16)
     assert found == 1 and st.found_inf == 1 and st.step == 0
     assert st.beta1_pow == 1.0 and st.beta2_pow == 1.0
     assert (w == 1).all() and (m == 0.5).all() and (v == 0.25).all() and (w16 == 7).all()
