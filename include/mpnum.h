@@ -201,6 +201,12 @@ typedef struct {
 /* Host helper: scale = scale_inv = 1, amax = 0, pos = 0, internals zero. */
 MP_API void mp_fp8_meta_init(mp_fp8_meta* host_meta);
 
+/* amax_algo of the FP8 casts: the next scale comes from the maximum of the
+ * history ring (the default of [FP8-TE] "Delayed Scaling 동작 원리"), or from
+ * the latest amax alone ([FP8-TE] "도입 체크리스트": most_recent, to follow
+ * fast changes). */
+enum { MP_AMAX_HISTORY_MAX = 0, MP_AMAX_MOST_RECENT = 1 };
+
 /* fp8_cast_delayed — one delayed-scaling cast ([FP8-TE] "Delayed Scaling 동작
  * 원리", "E4M3 vs E5M2", "FP8이 어려운 이유"; [MPT-ko] "FP8 혼합 정밀도").
  * Reads x once.  For each of the n elements of x (x_dtype MP_F32, MP_F16 or
@@ -209,14 +215,26 @@ MP_API void mp_fp8_meta_init(mp_fp8_meta* host_meta);
  * maximum, infinities included, become the signed maximum; NaN becomes 0x7F.
  * In the same pass amax = max |x| (NaN if any element is NaN).  Then
  * d_meta->amax = amax, d_history[p] = amax with p = pos mod history_len,
- * pos = (p + 1) % history_len,
- * and if H = max(d_history) is finite and > 0 the next scale is
- * fp8_max / (margin * H) (kept only if finite and > 0), scale_inv = 1/scale.
- * d_history: history_len FP32 entries (1..65536), zero-initialised by the
- * caller, non-negative.  x and y 16-byte aligned. */
+ * pos = (p + 1) % history_len, and if H = max(d_history) (amax_algo
+ * MP_AMAX_HISTORY_MAX) or H = amax (MP_AMAX_MOST_RECENT) is finite and > 0
+ * the next scale is fp8_max / (margin * H) (kept only if finite and > 0),
+ * scale_inv = 1/scale.  d_history: history_len FP32 entries (1..65536),
+ * zero-initialised by the caller, non-negative.  x and y 16-byte aligned.
+ * One kernel launch. */
 MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
                                   mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
-                                  int32_t history_len, float margin, void* stream);
+                                  int32_t history_len, float margin, int32_t amax_algo, void* stream);
+
+/* fp8_cast_transpose_delayed — fp8_cast_delayed of a [rows, cols] tensor that
+ * also writes y_t [cols, rows] = transpose(y) from the same single read: the
+ * backward GEMMs use the transposed operand ([NVFP4] §2.2 item 3 on the
+ * transposed tensors of the backward pass).  Same scaling, amax and history
+ * semantics; rows % 16 == 0 and cols % 16 == 0; x, y, y_t 16-byte aligned.
+ * One kernel launch. */
+MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
+                                            void* y, void* y_t, mp_dtype fp8_dtype, mp_fp8_meta* d_meta,
+                                            float* d_history, int32_t history_len, float margin,
+                                            int32_t amax_algo, void* stream);
 
 /* =========================================================================
  * 3. NVFP4 quantisation and the random Hadamard transform

@@ -100,7 +100,8 @@ def _load() -> ctypes.CDLL:
         "mp_adamw_check": (I32, [P, I32, I32, P, P, P, S, P]),
         "mp_adamw_apply": (I32, [P, I32, I32, I32, P, P, P]),
         "loss_scale_update": (I32, [P, P, P]),
-        "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, P]),
+        "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, I32, P]),
+        "fp8_cast_transpose_delayed": (I32, [P, I32, I64, I64, P, P, I32, P, P, I32, F, I32, P]),
         "nvfp4_workspace_size": (S, []),
         "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
         "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
@@ -279,12 +280,26 @@ def loss_scale_update(state, cfg: ScalerCfg, stream=None) -> None:
     _check("loss_scale_update", lib.loss_scale_update(_ptr(state), ctypes.byref(cfg), _stream(stream)))
 
 
+MP_AMAX_HISTORY_MAX, MP_AMAX_MOST_RECENT = 0, 1
+
+
 def fp8_cast_delayed(x, y, fp8_dtype: int, meta, history, margin: float = 1.0, stream=None,
-                     n: int | None = None) -> None:
+                     n: int | None = None, amax_algo: int = MP_AMAX_HISTORY_MAX) -> None:
     """y: uint8 (or float8) tensor with x.numel() elements; history: float32 device tensor."""
     _check("fp8_cast_delayed",
            lib.fp8_cast_delayed(_ptr(x), _dtype_code(x), x.numel() if n is None else n, _ptr(y), fp8_dtype,
-                                _ptr(meta), _ptr(history), history.numel(), float(margin), _stream(stream)))
+                                _ptr(meta), _ptr(history), history.numel(), float(margin), amax_algo,
+                                _stream(stream)))
+
+
+def fp8_cast_transpose_delayed(x, y, y_t, fp8_dtype: int, meta, history, margin: float = 1.0,
+                               amax_algo: int = MP_AMAX_HISTORY_MAX, stream=None) -> None:
+    """x: [rows, cols]; y: rows*cols bytes; y_t: cols*rows bytes (the transpose)."""
+    rows, cols = x.shape
+    _check("fp8_cast_transpose_delayed",
+           lib.fp8_cast_transpose_delayed(_ptr(x), _dtype_code(x), rows, cols, _ptr(y), _ptr(y_t), fp8_dtype,
+                                          _ptr(meta), _ptr(history), history.numel(), float(margin), amax_algo,
+                                          _stream(stream)))
 
 
 def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *, block_2d: bool = False,
@@ -322,6 +337,7 @@ __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
+    "fp8_cast_transpose_delayed", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",

@@ -77,89 +77,35 @@ __device__ __forceinline__ uint32_t hist_key(float h) {
   return (h != h) ? 0x7FC00000u : (h > 0.0f ? __float_as_uint(h) : 0u);
 }
 
-template <int XT, bool E5M2>
-__global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ x, int64_t n,
-                                                       uint8_t* __restrict__ y, mp_fp8_meta* meta,
-                                                       float* hist, int32_t hist_len, float margin) {
-  constexpr int U = unroll_of<XT>();
-  __shared__ uint32_t red[32];
-  __shared__ int is_last;
-  const float scale = meta->scale;
-  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
+// CTA 0, at the start of a history-max cast: fold the history entries this
+// call does not overwrite into meta->internal_hrest.
+__device__ __forceinline__ void fold_history_rest(mp_fp8_meta* meta, const float* hist, int32_t hist_len,
+                                                  int32_t slot, uint32_t* red) {
+  uint32_t hm = 0;
+  for (int i = threadIdx.x; i < hist_len; i += blockDim.x)
+    if (i != slot) hm = max(hm, hist_key(hist[i]));
+  hm = block_max_u32(hm, red);
+  if (threadIdx.x == 0) meta->internal_hrest = hm;
+  __syncthreads();  // red is reused
+}
 
-  // CTA 0 folds the history entries this call does not overwrite while the
-  // stream runs, so the last CTA only has to combine them with this amax.
-  if (blockIdx.x == 0) {
-    uint32_t hm = 0;
-    for (int i = threadIdx.x; i < hist_len; i += kThreads)
-      if (i != slot) hm = max(hm, hist_key(hist[i]));
-    hm = block_max_u32(hm, red);
-    if (threadIdx.x == 0) meta->internal_hrest = hm;
-    __syncthreads();  // red is reused below
-  }
-
-  float acc = 0.0f;
-  const int64_t nvec = n / kElems;
-  const int64_t step = (int64_t)gridDim.x * kThreads * U;
-  for (int64_t v0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; v0 < nvec; v0 += step) {
-    uint4 raw[U][4];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t vec = v0 + (int64_t)u * kThreads;
-      if (vec < nvec) load_raw<XT>(x, vec, raw[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t vec = v0 + (int64_t)u * kThreads;
-      if (vec >= nvec) continue;
-      float vmax = 0.0f;
-      uint32_t h[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float2 f = pair_of<XT>(raw[u], k);
-        vmax = max_abs_nan(vmax, f.x);
-        vmax = max_abs_nan(vmax, f.y);
-        h[k] = cast_pair<E5M2>(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
-      }
-      uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-      if (__builtin_expect(vmax != vmax, 0)) {  // a NaN input: its byte is 0x7F
-        uint8_t* ob = reinterpret_cast<uint8_t*>(&o);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 f = pair_of<XT>(raw[u], k);
-          if (f.x != f.x) ob[2 * k] = 0x7F;
-          if (f.y != f.y) ob[2 * k + 1] = 0x7F;
-        }
-      }
-      st_cs(y + vec * kElems, o);
-      acc = max_abs_nan(acc, vmax);
-    }
-  }
-  // Tail elements (n % 16) go to the first CTA.
-  if (blockIdx.x == 0) {
-    const int64_t i = nvec * kElems + threadIdx.x;
-    if (i < n) {
-      const float a = load1<XT>(x, i);
-      acc = max_abs_nan(acc, a);
-      uint32_t b = cast_pair<E5M2>(__fmul_rn(a, scale), 0.0f) & 0xFFu;
-      if (a != a) b = 0x7F;
-      y[i] = (uint8_t)b;
-    }
-  }
-
+// End of every CTA: fold its amax into the meta word; the last CTA (atomic
+// ticket, no waiting) writes the ring slot and derives the next scale from
+// max(history) (algo 0) or from this amax alone (algo 1).
+template <bool E5M2>
+__device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32_t hist_len, int32_t slot,
+                                           float margin, int32_t algo, float acc, uint32_t* red, int* is_last) {
   const uint32_t cta = block_max_u32(amax_bits(acc), red);
   if (threadIdx.x == 0) {
     atomicMax(&meta->internal_amax, cta);
     __threadfence();
-    is_last = atomicAdd(&meta->internal_ticket, 1u) == gridDim.x - 1;
+    *is_last = atomicAdd(&meta->internal_ticket, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!is_last || threadIdx.x != 0) return;
-
-  // Last CTA: record this step's amax and derive the next scale.
+  if (!*is_last || threadIdx.x != 0) return;
   __threadfence();
   const uint32_t ab = atomicExch(&meta->internal_amax, 0u);
-  const uint32_t hm = max(*reinterpret_cast<volatile uint32_t*>(&meta->internal_hrest), ab);
+  const uint32_t hm = algo == 1 ? ab : max(*reinterpret_cast<volatile uint32_t*>(&meta->internal_hrest), ab);
   meta->internal_ticket = 0;
   const float amax = __uint_as_float(ab);
   meta->amax = amax;
@@ -178,22 +124,163 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
   }
 }
 
+// Casts one raw 16-element vector; returns the 16 output bytes and the
+// vector's NaN-propagating max |x| in *vmax.
+template <int XT, bool E5M2>
+__device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out) {
+  float vmax = 0.0f;
+  uint32_t h[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float2 f = pair_of<XT>(raw, k);
+    vmax = max_abs_nan(vmax, f.x);
+    vmax = max_abs_nan(vmax, f.y);
+    h[k] = cast_pair<E5M2>(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
+  }
+  uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
+  if (__builtin_expect(vmax != vmax, 0)) {  // a NaN input: its byte is 0x7F
+    uint8_t* ob = reinterpret_cast<uint8_t*>(&o);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float2 f = pair_of<XT>(raw, k);
+      if (f.x != f.x) ob[2 * k] = 0x7F;
+      if (f.y != f.y) ob[2 * k + 1] = 0x7F;
+    }
+  }
+  *vmax_out = vmax;
+  return o;
+}
+
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ x, int64_t n,
+                                                       uint8_t* __restrict__ y, mp_fp8_meta* meta,
+                                                       float* hist, int32_t hist_len, float margin, int32_t algo) {
+  constexpr int U = unroll_of<XT>();
+  __shared__ uint32_t red[32];
+  __shared__ int is_last;
+  const float scale = meta->scale;
+  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
+  if (blockIdx.x == 0 && algo == 0) fold_history_rest(meta, hist, hist_len, slot, red);
+
+  float acc = 0.0f;
+  const int64_t nvec = n / kElems;
+  const int64_t step = (int64_t)gridDim.x * kThreads * U;
+  for (int64_t v0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; v0 < nvec; v0 += step) {
+    uint4 raw[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t vec = v0 + (int64_t)u * kThreads;
+      if (vec < nvec) load_raw<XT>(x, vec, raw[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t vec = v0 + (int64_t)u * kThreads;
+      if (vec >= nvec) continue;
+      float vmax;
+      st_cs(y + vec * kElems, cast16<XT, E5M2>(raw[u], scale, &vmax));
+      acc = max_abs_nan(acc, vmax);
+    }
+  }
+  // Tail elements (n % 16) go to the first CTA.
+  if (blockIdx.x == 0) {
+    const int64_t i = nvec * kElems + threadIdx.x;
+    if (i < n) {
+      const float a = load1<XT>(x, i);
+      acc = max_abs_nan(acc, a);
+      uint32_t b = cast_pair<E5M2>(__fmul_rn(a, scale), 0.0f) & 0xFFu;
+      if (a != a) b = 0x7F;
+      y[i] = (uint8_t)b;
+    }
+  }
+  fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
+}
+
+// Cast of a [rows, cols] tensor that also writes the transposed bytes
+// y_t [cols, rows] from the same read: a CTA takes a 64 x 64 tile, casts it
+// (each thread one 16-element row segment), stores the rows of y, stages the
+// bytes in shared memory and stores 16-byte column segments of y_t.
+constexpr int kTT = 64;  // tile edge
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(kThreads) void k_fp8_cast_t(const void* __restrict__ x, int64_t rows, int64_t cols,
+                                                         uint8_t* __restrict__ y, uint8_t* __restrict__ y_t,
+                                                         mp_fp8_meta* meta, float* hist, int32_t hist_len,
+                                                         float margin, int32_t algo) {
+  __shared__ uint32_t red[32];
+  __shared__ int is_last;
+  __shared__ __align__(16) uint8_t tile[kTT][kTT + 16];  // 80-byte pitch: 16-byte row segments stay aligned
+  const float scale = meta->scale;
+  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;
+  if (blockIdx.x == 0 && algo == 0) fold_history_rest(meta, hist, hist_len, slot, red);
+  const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
+  const int lr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;  // row in tile, column segment
+  float acc = 0.0f;
+  for (int64_t tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
+    const int64_t r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
+    const int64_t row = r0 + lr, col = c0 + seg;
+    if (row < rows && col < cols) {
+      uint4 raw[4];
+      load_raw<XT>(x, (row * cols + col) / kElems, raw);
+      float vmax;
+      const uint4 o = cast16<XT, E5M2>(raw, scale, &vmax);
+      acc = max_abs_nan(acc, vmax);
+      st_cs(y + row * cols + col, o);
+      *reinterpret_cast<uint4*>(&tile[lr][seg]) = o;
+    }
+    __syncthreads();
+    // transposed: thread handles column lr of the tile, rows seg .. seg + 15
+    const int64_t tcol = c0 + lr, trow = r0 + seg;
+    if (tcol < cols && trow < rows) {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        w[q] = (uint32_t)tile[seg + 4 * q][lr] | ((uint32_t)tile[seg + 4 * q + 1][lr] << 8) |
+               ((uint32_t)tile[seg + 4 * q + 2][lr] << 16) | ((uint32_t)tile[seg + 4 * q + 3][lr] << 24);
+      st_cs(y_t + tcol * rows + trow, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+    __syncthreads();  // the tile is rewritten by the next iteration
+  }
+  fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
+}
+
+template <typename K>
+int occ_of(K kernel) {
+  int o = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kThreads, 0) != cudaSuccess || o < 1) o = 1;
+  return o;
+}
+
 template <int XT, bool E5M2>
 mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float* hist, int32_t len,
-                 float margin, cudaStream_t s) {
-  static int occ = 0;
-  if (occ == 0) {
-    int o = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k_fp8_cast<XT, E5M2>, kThreads, 0) != cudaSuccess || o < 1)
-      o = 1;
-    occ = o;
-  }
+                 float margin, int32_t algo, cudaStream_t s) {
+  static const int occ = occ_of(k_fp8_cast<XT, E5M2>);
   const int64_t nvec = n / kElems;
   constexpr int U = unroll_of<XT>();
   const int64_t ctas = (nvec + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
-  k_fp8_cast<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin);
+  k_fp8_cast<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin, algo);
   note_launches(1);
   return launch_status();
+}
+
+template <int XT, bool E5M2>
+mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_t* y_t, mp_fp8_meta* meta,
+                   float* hist, int32_t len, float margin, int32_t algo, cudaStream_t s) {
+  static const int occ = occ_of(k_fp8_cast_t<XT, E5M2>);
+  const int64_t tiles = ((rows + kTT - 1) / kTT) * ((cols + kTT - 1) / kTT);
+  k_fp8_cast_t<XT, E5M2><<<grid_for(tiles, occ), kThreads, 0, s>>>(x, rows, cols, y, y_t, meta, hist, len, margin,
+                                                                    algo);
+  note_launches(1);
+  return launch_status();
+}
+
+mp_status check_common(mp_dtype x_dtype, mp_dtype fp8_dtype, const mp_fp8_meta* d_meta, const float* d_history,
+                       int32_t history_len, float margin, int32_t amax_algo) {
+  if (!d_meta || !d_history || history_len < 1 || history_len > 65536) return MP_EINVAL;
+  if (x_dtype != MP_F32 && x_dtype != MP_F16 && x_dtype != MP_BF16) return MP_EINVAL;
+  if (fp8_dtype != MP_E4M3 && fp8_dtype != MP_E5M2) return MP_EINVAL;
+  if (amax_algo != 0 && amax_algo != 1) return MP_EINVAL;
+  if (!(margin > 0.0f) || !(margin - margin == 0.0f)) return MP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(d_meta) & 15u) || (reinterpret_cast<uintptr_t>(d_history) & 3u)) return MP_EALIGN;
+  return MP_OK;
 }
 
 }  // namespace
@@ -201,28 +288,53 @@ mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float*
 
 extern "C" MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
                                              mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
-                                             int32_t history_len, float margin, void* stream) {
+                                             int32_t history_len, float margin, int32_t amax_algo, void* stream) {
   using namespace mp;
-  if (n < 0 || !d_meta || !d_history || history_len < 1 || history_len > 65536) return MP_EINVAL;
-  if (n > 0 && (!x || !y)) return MP_EINVAL;
-  if (x_dtype != MP_F32 && x_dtype != MP_F16 && x_dtype != MP_BF16) return MP_EINVAL;
-  if (fp8_dtype != MP_E4M3 && fp8_dtype != MP_E5M2) return MP_EINVAL;
-  if (!(margin > 0.0f) || !(margin - margin == 0.0f)) return MP_EINVAL;
-  if ((n > 0 && (!aligned16(x) || !aligned16(y))) || (reinterpret_cast<uintptr_t>(d_meta) & 15u) ||
-      (reinterpret_cast<uintptr_t>(d_history) & 3u))
-    return MP_EALIGN;
+  if (n < 0 || (n > 0 && (!x || !y))) return MP_EINVAL;
+  const mp_status rc = check_common(x_dtype, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo);
+  if (rc != MP_OK) return rc;
+  if (n > 0 && (!aligned16(x) || !aligned16(y))) return MP_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* yb = static_cast<uint8_t*>(y);
   const bool e5 = fp8_dtype == MP_E5M2;
   switch (x_dtype) {
     case MP_F32:
-      return e5 ? launch<XF32, true>(x, n, yb, d_meta, d_history, history_len, margin, s)
-                : launch<XF32, false>(x, n, yb, d_meta, d_history, history_len, margin, s);
+      return e5 ? launch<XF32, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch<XF32, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
     case MP_F16:
-      return e5 ? launch<XF16, true>(x, n, yb, d_meta, d_history, history_len, margin, s)
-                : launch<XF16, false>(x, n, yb, d_meta, d_history, history_len, margin, s);
+      return e5 ? launch<XF16, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch<XF16, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
     default:
-      return e5 ? launch<XBF16, true>(x, n, yb, d_meta, d_history, history_len, margin, s)
-                : launch<XBF16, false>(x, n, yb, d_meta, d_history, history_len, margin, s);
+      return e5 ? launch<XBF16, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch<XBF16, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
+  }
+}
+
+extern "C" MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
+                                                       void* y, void* y_t, mp_dtype fp8_dtype, mp_fp8_meta* d_meta,
+                                                       float* d_history, int32_t history_len, float margin,
+                                                       int32_t amax_algo, void* stream) {
+  using namespace mp;
+  if (rows < 0 || cols < 0) return MP_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x || !y || !y_t)) return MP_EINVAL;
+  const mp_status rc = check_common(x_dtype, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo);
+  if (rc != MP_OK) return rc;
+  if (rows % 16 != 0 || cols % 16 != 0) return MP_ESHAPE;
+  if (n > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(y_t))) return MP_EALIGN;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t *yb = static_cast<uint8_t*>(y), *ytb = static_cast<uint8_t*>(y_t);
+  const bool e5 = fp8_dtype == MP_E5M2;
+  switch (x_dtype) {
+    case MP_F32:
+      return e5 ? launch_t<XF32, true>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch_t<XF32, false>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s);
+    case MP_F16:
+      return e5 ? launch_t<XF16, true>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch_t<XF16, false>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s);
+    default:
+      return e5 ? launch_t<XBF16, true>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s)
+                : launch_t<XBF16, false>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo,
+                                         s);
   }
 }

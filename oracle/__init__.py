@@ -117,8 +117,9 @@ def lib() -> ctypes.CDLL:
             "orc_clip_coef": (F, [ctypes.c_double, F]),
             "orc_fp8_cast_one": (U8, [F, F, ctypes.c_int]),
             "orc_fp8_cast_array": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, F]),
-            "orc_fp8_history_update": (None, [P, P, I32, F, F, ctypes.c_int]),
-            "orc_fp8_cast_delayed": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, P, P, I32, F]),
+            "orc_fp8_history_update": (None, [P, P, I32, F, F, ctypes.c_int, ctypes.c_int]),
+            "orc_fp8_cast_delayed": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, P, P, I32, F, ctypes.c_int]),
+            "orc_transpose_u8": (None, [P, I64, I64, P]),
             "orc_nvfp4_prepare": (ctypes.c_int, [P, I64, I64, ctypes.c_int, U16, P]),
             "orc_nvfp4_tensor_scale": (F, [F, P]),
             "orc_nvfp4_encode_rows": (
@@ -246,20 +247,34 @@ def fp8_cast_array(x: np.ndarray, x_fmt: int, fmt: int, scale: float) -> np.ndar
     return y
 
 
-def fp8_history_update(meta: Fp8Meta, history: np.ndarray, margin: float, amax_v: float, fmt: int) -> None:
+AMAX_HISTORY_MAX, AMAX_MOST_RECENT = 0, 1
+
+
+def fp8_history_update(meta: Fp8Meta, history: np.ndarray, margin: float, amax_v: float, fmt: int,
+                       amax_algo: int = AMAX_HISTORY_MAX) -> None:
     assert history.dtype == np.float32
     lib().orc_fp8_history_update(
-        ctypes.byref(meta), _p(history), history.size, np.float32(margin), np.float32(amax_v), fmt
+        ctypes.byref(meta), _p(history), history.size, np.float32(margin), np.float32(amax_v), fmt, amax_algo
     )
 
 
-def fp8_cast_delayed(x: np.ndarray, x_fmt: int, fmt: int, meta: Fp8Meta, history: np.ndarray, margin: float):
+def fp8_cast_delayed(x: np.ndarray, x_fmt: int, fmt: int, meta: Fp8Meta, history: np.ndarray, margin: float,
+                     amax_algo: int = AMAX_HISTORY_MAX):
     x = np.ascontiguousarray(x, dtype=_NP[x_fmt])
     y = np.empty(x.shape, dtype=np.uint8)
     lib().orc_fp8_cast_delayed(
-        _p(x), x_fmt, x.size, _p(y), fmt, ctypes.byref(meta), _p(history), history.size, np.float32(margin)
+        _p(x), x_fmt, x.size, _p(y), fmt, ctypes.byref(meta), _p(history), history.size, np.float32(margin),
+        amax_algo
     )
     return y
+
+
+def transpose_u8(y: np.ndarray) -> np.ndarray:
+    y = np.ascontiguousarray(y, dtype=np.uint8)
+    rows, cols = y.shape
+    out = np.empty((cols, rows), dtype=np.uint8)
+    lib().orc_transpose_u8(_p(y), rows, cols, _p(out))
+    return out
 
 
 # --- NVFP4 -----------------------------------------------------------------------

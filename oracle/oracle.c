@@ -441,16 +441,20 @@ void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt
 }
 
 void orc_fp8_history_update(orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
-                            float amax, int fmt) {
+                            float amax, int fmt, int amax_algo) {
   meta->amax = amax;
   /* reading R9b: the ring slot is pos taken modulo the ring length */
   int32_t pos = ((meta->pos % hist_len) + hist_len) % hist_len;
   history[pos] = amax;
   meta->pos = (pos + 1) % hist_len;
   float hmax = 0.0f;
-  for (int32_t i = 0; i < hist_len; ++i) {
-    if (isnan(history[i])) { hmax = history[i]; break; }
-    if (history[i] > hmax) hmax = history[i];
+  if (amax_algo == 1) {
+    hmax = amax > 0.0f || isnan(amax) ? amax : 0.0f;
+  } else {
+    for (int32_t i = 0; i < hist_len; ++i) {
+      if (isnan(history[i])) { hmax = history[i]; break; }
+      if (history[i] > hmax) hmax = history[i];
+    }
   }
   if (!(isfinite(hmax) && hmax > 0.0f)) return;
   float denom = margin * hmax;
@@ -463,10 +467,16 @@ void orc_fp8_history_update(orc_fp8_meta* meta, float* history, int32_t hist_len
 }
 
 void orc_fp8_cast_delayed(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt,
-                          orc_fp8_meta* meta, float* history, int32_t hist_len, float margin) {
+                          orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
+                          int amax_algo) {
   orc_fp8_cast_array(x, x_fmt, n, y, fmt, meta->scale);
   float amax = orc_amax(x, x_fmt, n);
-  orc_fp8_history_update(meta, history, hist_len, margin, amax, fmt);
+  orc_fp8_history_update(meta, history, hist_len, margin, amax, fmt, amax_algo);
+}
+
+void orc_transpose_u8(const uint8_t* y, int64_t rows, int64_t cols, uint8_t* y_t) {
+  for (int64_t r = 0; r < rows; ++r)
+    for (int64_t c = 0; c < cols; ++c) y_t[c * rows + r] = y[r * cols + c];
 }
 
 /* ---------------------------------------------------------------------------

@@ -143,12 +143,17 @@ typedef struct {
 uint8_t orc_fp8_cast_one(float x, float scale, int fmt);
 /* Casts n elements with meta->scale; does not touch meta. */
 void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt, float scale);
-/* Records amax in the ring and derives the next scale. */
+/* Records amax in the ring and derives the next scale from max(history)
+ * (amax_algo 0) or from this amax alone (amax_algo 1, "most_recent",
+ * [FP8-TE] "도입 체크리스트"). */
 void orc_fp8_history_update(orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
-                            float amax, int fmt);
+                            float amax, int fmt, int amax_algo);
 /* One full iteration: cast with the current scale, amax, ring write, new scale. */
 void orc_fp8_cast_delayed(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt,
-                          orc_fp8_meta* meta, float* history, int32_t hist_len, float margin);
+                          orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
+                          int amax_algo);
+/* y_t[c][r] = y[r][c] for a [rows][cols] byte matrix. */
+void orc_transpose_u8(const uint8_t* y, int64_t rows, int64_t cols, uint8_t* y_t);
 
 /* ---- NVFP4 quantisation ([NVFP4] §2.1, §2.2) ---------------------------------- */
 /* x' = x or RHT(x), as FP32. */

@@ -190,3 +190,85 @@ def test_fp8_workload_full_size_sampled(which):
         sat += int(top.sum().item())
     if which == "act":
         assert sat > 0  # the drifting std makes the delayed scale lag: saturation happens
+
+
+# ---- most_recent amax and the transposed output ----------------------------------
+
+
+def test_most_recent_sequence():
+    c = W.TINY_FP8
+    meta = M.new_fp8_meta()
+    hist = torch.zeros(c.hist_len, dtype=torch.float32, device="cuda")
+    om, oh = O.new_fp8_meta(), np.zeros(c.hist_len, np.float32)
+    for k in range(8):
+        r = synth.recipe(c.seed, 100 + k, float(2.0 ** (k % 5 - 2)))
+        x = synth.fill(r, synth.BF16, 65536 + 3)
+        y = torch.empty(x.size, dtype=torch.uint8, device="cuda")
+        M.fp8_cast_delayed(to_dev(x, torch.bfloat16), y, M.MP_E4M3, meta, hist, 1.5, amax_algo=M.MP_AMAX_MOST_RECENT)
+        ref = O.fp8_cast_delayed(x, O.BF16, O.E4M3, om, oh, 1.5, O.AMAX_MOST_RECENT)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(y.cpu().numpy(), ref)
+        assert_meta_equal(M.read_fp8_meta(meta), om)
+        np.testing.assert_array_equal(hist.cpu().numpy().view(np.uint32), oh.view(np.uint32))
+
+
+def cast_t(xt, fmt, meta, hist, algo=0):
+    rows, cols = xt.shape
+    y = torch.full((rows * cols,), 0xCC, dtype=torch.uint8, device="cuda")
+    yt = torch.full((cols * rows,), 0xCC, dtype=torch.uint8, device="cuda")
+    M.fp8_cast_transpose_delayed(xt, y, yt, fmt, meta, hist, 1.0, algo)
+    torch.cuda.synchronize()
+    return y.cpu().numpy().reshape(rows, cols), yt.cpu().numpy().reshape(cols, rows)
+
+
+@pytest.mark.parametrize("shape", [(16, 16), (64, 64), (80, 144), (48, 1040), (1024, 1040)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("fmt", [M.MP_E4M3, M.MP_E5M2])
+def test_cast_transpose_small(shape, dtype, fmt):
+    rows, cols = shape
+    xf = synth.fill(synth.recipe(80, rows, 3.0, 0.01, 100.0, synth.OUT_SCALE), synth.F32, rows * cols)
+    xf[:3] = [np.inf, np.nan, -0.0]
+    if dtype == torch.float32:
+        x = xf
+        xt = to_dev(x).reshape(rows, cols)
+    else:
+        fmt16 = O.BF16 if dtype == torch.bfloat16 else O.F16
+        x = O.convert(xf, O.F32, fmt16)
+        xt = to_dev(x, dtype).reshape(rows, cols)
+    meta = M.new_fp8_meta()
+    hist = torch.zeros(4, dtype=torch.float32, device="cuda")
+    set_meta(meta, 13.0)
+    y, yt = cast_t(xt, fmt, meta, hist)
+    ref = O.fp8_cast_array(x, XFMT[dtype], FMT[fmt], 13.0).reshape(rows, cols)
+    np.testing.assert_array_equal(y, ref)
+    np.testing.assert_array_equal(yt, O.transpose_u8(ref))
+    om = O.new_fp8_meta()
+    om.scale, om.scale_inv = 13.0, float(np.float32(1) / np.float32(13))
+    oh = np.zeros(4, np.float32)
+    O.fp8_history_update(om, oh, 1.0, O.amax(x, XFMT[dtype]), FMT[fmt])
+    assert_meta_equal(M.read_fp8_meta(meta), om)
+
+
+def test_cast_transpose_full_size_sequence():
+    c = W.FP8
+    meta = M.new_fp8_meta()
+    hist = torch.zeros(c.hist_len, dtype=torch.float32, device="cuda")
+    om, oh = O.new_fp8_meta(), np.zeros(c.hist_len, np.float32)
+    x = torch.empty((c.rows, c.cols), dtype=torch.bfloat16, device="cuda")
+    for k in range(3):
+        synth.fill_device(c.act_recipe(k), synth.BF16, x)
+        y, yt = cast_t(x, M.MP_E4M3, meta, hist)
+        xh = to_host(x, np.uint16).reshape(c.rows, c.cols)
+        ref = O.fp8_cast_delayed(xh, O.BF16, O.E4M3, om, oh, c.margin)
+        assert np.array_equal(y, ref.reshape(c.rows, c.cols)), f"iteration {k}"
+        assert np.array_equal(yt, ref.reshape(c.rows, c.cols).T), f"iteration {k} transposed"
+        assert_meta_equal(M.read_fp8_meta(meta), om)
+
+
+def test_cast_transpose_argument_errors():
+    x = torch.zeros((16, 24), dtype=torch.bfloat16, device="cuda")
+    y = torch.zeros(16 * 32, dtype=torch.uint8, device="cuda")
+    meta, hist = M.new_fp8_meta(), torch.zeros(4, device="cuda")
+    with pytest.raises(M.MpError) as e:
+        M.fp8_cast_transpose_delayed(x, y, y, M.MP_E4M3, meta, hist)
+    assert e.value.status == M.MP_ESHAPE

@@ -72,10 +72,14 @@ def test_argument_validation_without_gpu(M):
     assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(neg), 16, None, 0, None) == M.MP_EINVAL
     cfg = M.ScalerCfg(2.0, 0.5, 0, 1)
     assert L.loss_scale_update(16, ctypes.byref(cfg), None) == M.MP_EINVAL
-    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_F16, 16, 16, 4, 1.0, None) == M.MP_EINVAL
-    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 0, 1.0, None) == M.MP_EINVAL
-    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 0.0, None) == M.MP_EINVAL
-    assert L.fp8_cast_delayed(8, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, None) == M.MP_EALIGN
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_F16, 16, 16, 4, 1.0, 0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 0, 1.0, 0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 0.0, 0, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 2, None) == M.MP_EINVAL
+    assert L.fp8_cast_delayed(8, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_EALIGN
+    t = L.fp8_cast_transpose_delayed
+    assert t(16, M.MP_BF16, 16, 24, 16, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_ESHAPE
+    assert t(16, M.MP_BF16, 16, 32, 16, 8, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_EALIGN
     q = L.nvfp4_quantize
     assert q(16, 2, 24, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
     assert q(16, 8, 32, 1, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE

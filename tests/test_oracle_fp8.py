@@ -115,3 +115,21 @@ def test_ring_slot_is_taken_modulo_the_length():
     hist = np.zeros(4, np.float32)
     O.fp8_cast_delayed(one_hot(32, 0, 5.0), O.BF16, O.E4M3, meta, hist, 1.0)
     assert hist[1] == 5.0 and meta.pos == 2
+
+
+@pytest.mark.parametrize("fmt,fmax", [(O.E4M3, 448.0), (O.E5M2, 57344.0)])
+def test_most_recent_uses_only_the_latest_amax(fmt, fmax):
+    # [FP8-TE] checklist: amax_compute_algo = most_recent follows fast changes.
+    meta = O.new_fp8_meta()
+    hist = np.zeros(8, np.float32)
+    for k, a in enumerate([64.0, 2.0, 4.0, 0.5, 100.0, 1.0]):
+        O.fp8_cast_delayed(one_hot(64, k, a), O.BF16, fmt, meta, hist, 2.0, O.AMAX_MOST_RECENT)
+        assert meta.scale == np.float32(fmax) / (np.float32(2.0) * np.float32(a))
+        assert hist[k] == a  # the ring is still recorded
+    O.fp8_cast_delayed(bf16(np.zeros(16)), O.BF16, fmt, meta, hist, 2.0, O.AMAX_MOST_RECENT)
+    assert meta.scale == np.float32(fmax) / np.float32(2.0)  # zero amax keeps the scale
+
+
+def test_transpose_matches_numpy():
+    y = np.random.default_rng(1).integers(0, 256, size=(48, 80)).astype(np.uint8)
+    np.testing.assert_array_equal(O.transpose_u8(y), y.T)
