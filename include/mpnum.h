@@ -236,6 +236,21 @@ MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int
                                             float* d_history, int32_t history_len, float margin,
                                             int32_t amax_algo, void* stream);
 
+/* fp8_quantize_blockwise — fine-grained FP8 with scales computed on the fly
+ * per block, no history ([FP8-TE] "DeepSeek-V3 FP8 학습 사례": activations in
+ * 1x128 tiles, weights in 128x128 blocks, E4M3 throughout; [MPT-ko] "FP8 혼합
+ * 정밀도").  For each block (block_rows x block_cols = 1x128 or 128x128;
+ * blocks at the right and bottom edges may be partial): amax = max |x| (NaN
+ * if any is NaN), scales[block] = amax / fp8_max (the quiet NaN 0x7FC00000
+ * for a block holding a NaN; FP32, row-major
+ * [ceil(rows/br)][ceil(cols/bc)]), and every element
+ * y = saturate(RNE(fp32(x) * r)) with r = fp8_max / amax if amax is finite
+ * and > 0, else r = 0 (a NaN product gives 0x7F).  Each block is read once.
+ * cols % 16 == 0; x, y 16-byte aligned.  One kernel launch. */
+MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
+                                        int32_t block_rows, int32_t block_cols, void* y, mp_dtype fp8_dtype,
+                                        float* scales, void* stream);
+
 /* =========================================================================
  * 3. NVFP4 quantisation and the random Hadamard transform
  * ========================================================================= */

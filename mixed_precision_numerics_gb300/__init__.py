@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "loss_scale_update": (I32, [P, P, P]),
         "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, I32, P]),
         "fp8_cast_transpose_delayed": (I32, [P, I32, I64, I64, P, P, I32, P, P, I32, F, I32, P]),
+        "fp8_quantize_blockwise": (I32, [P, I32, I64, I64, I32, I32, P, I32, P, P]),
         "nvfp4_workspace_size": (S, []),
         "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
         "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
@@ -302,6 +303,15 @@ def fp8_cast_transpose_delayed(x, y, y_t, fp8_dtype: int, meta, history, margin:
                                           _stream(stream)))
 
 
+def fp8_quantize_blockwise(x, y, scales, block_rows: int = 1, block_cols: int = 128, fp8_dtype: int = MP_E4M3,
+                           stream=None) -> None:
+    """x: [rows, cols]; y: rows*cols bytes; scales: float32 [ceil(rows/br), ceil(cols/bc)]."""
+    rows, cols = x.shape
+    _check("fp8_quantize_blockwise",
+           lib.fp8_quantize_blockwise(_ptr(x), _dtype_code(x), rows, cols, block_rows, block_cols, _ptr(y), fp8_dtype,
+                                      _ptr(scales), _stream(stream)))
+
+
 def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *, block_2d: bool = False,
                    stochastic: bool = False, seed: int = 0, apply_rht: bool = False, sign_mask: int = 0,
                    dequant=None, rows: int | None = None, cols: int | None = None, stream=None) -> None:
@@ -337,7 +347,7 @@ __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
-    "fp8_cast_transpose_delayed", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
+    "fp8_cast_transpose_delayed", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",

@@ -124,27 +124,32 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
   }
 }
 
-// Casts one raw 16-element vector; returns the 16 output bytes and the
-// vector's NaN-propagating max |x| in *vmax.
+// Casts one raw 16-element vector with multiplier `scale`; returns the 16
+// output bytes and the vector's NaN-propagating max |x| in *vmax.  A NaN
+// product (a NaN input, or an infinite input times a zero multiplier) gives
+// 0x7F; the products are checked, not the inputs.
 template <int XT, bool E5M2>
 __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out) {
-  float vmax = 0.0f;
+  float vmax = 0.0f, pmax = 0.0f;
   uint32_t h[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const float2 f = pair_of<XT>(raw, k);
     vmax = max_abs_nan(vmax, f.x);
     vmax = max_abs_nan(vmax, f.y);
-    h[k] = cast_pair<E5M2>(__fmul_rn(f.x, scale), __fmul_rn(f.y, scale));
+    const float p0 = __fmul_rn(f.x, scale), p1 = __fmul_rn(f.y, scale);
+    pmax = max_abs_nan(pmax, p0);
+    pmax = max_abs_nan(pmax, p1);
+    h[k] = cast_pair<E5M2>(p0, p1);
   }
   uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-  if (__builtin_expect(vmax != vmax, 0)) {  // a NaN input: its byte is 0x7F
+  if (__builtin_expect(pmax != pmax, 0)) {
     uint8_t* ob = reinterpret_cast<uint8_t*>(&o);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float2 f = pair_of<XT>(raw, k);
-      if (f.x != f.x) ob[2 * k] = 0x7F;
-      if (f.y != f.y) ob[2 * k + 1] = 0x7F;
+      if (__fmul_rn(f.x, scale) != __fmul_rn(f.x, scale)) ob[2 * k] = 0x7F;
+      if (__fmul_rn(f.y, scale) != __fmul_rn(f.y, scale)) ob[2 * k + 1] = 0x7F;
     }
   }
   *vmax_out = vmax;
@@ -187,8 +192,9 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
     if (i < n) {
       const float a = load1<XT>(x, i);
       acc = max_abs_nan(acc, a);
-      uint32_t b = cast_pair<E5M2>(__fmul_rn(a, scale), 0.0f) & 0xFFu;
-      if (a != a) b = 0x7F;
+      const float p = __fmul_rn(a, scale);
+      uint32_t b = cast_pair<E5M2>(p, 0.0f) & 0xFFu;
+      if (p != p) b = 0x7F;
       y[i] = (uint8_t)b;
     }
   }
@@ -242,6 +248,105 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast_t(const void* __restrict_
   fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
 }
 
+// ---------------------------------------------------------------------------
+// Fine-grained FP8 with online block scales ([FP8-TE] "DeepSeek-V3 FP8 학습
+// 사례"; [MPT-ko] "FP8 혼합 정밀도"): each 1x128 tile or 128x128 block is read
+// once, its amax reduced on chip, s = amax / fp8_max stored, and its elements
+// cast with r = fp8_max / amax (0 if amax is zero or not finite).
+// ---------------------------------------------------------------------------
+template <bool E5M2>
+__device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
+  constexpr float fmax = E5M2 ? 57344.0f : 448.0f;
+  *s = (amax != amax) ? __uint_as_float(0x7FC00000u) : __fdiv_rn(amax, fmax);  // NaN block: quiet NaN
+  *r = (isfinite(amax) && amax > 0.0f) ? __fdiv_rn(fmax, amax) : 0.0f;
+}
+
+// 1 x 128 tiles: eight threads per tile (16 elements each), four tiles per
+// warp; the loop runs over warp-sized groups of tiles so that every lane
+// takes part in the width-8 shuffles.
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(kThreads) void k_fp8_block_1x128(const void* __restrict__ x, int64_t rows,
+                                                              int64_t cols, uint8_t* __restrict__ y,
+                                                              float* __restrict__ scales) {
+  const int64_t ntc = (cols + 127) / 128;
+  const int64_t ntiles = rows * ntc;
+  const int64_t nquads = (ntiles + 3) / 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 3, l8 = lane & 7;
+  const int64_t wstride = (int64_t)gridDim.x * (kThreads / 32);
+  for (int64_t q = (int64_t)blockIdx.x * (kThreads / 32) + warp; q < nquads; q += wstride) {
+    const int64_t tile = q * 4 + g;
+    const int64_t row = tile / ntc, tc = tile % ntc;
+    const int64_t col = tc * 128 + l8 * 16;
+    const bool valid = tile < ntiles && col < cols;
+    uint4 raw[4];
+    float vmax = 0.0f;
+    if (valid) {
+      load_raw<XT>(x, (row * cols + col) / kElems, raw);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 f = pair_of<XT>(raw, k);
+        vmax = max_abs_nan(vmax, f.x);
+        vmax = max_abs_nan(vmax, f.y);
+      }
+    }
+#pragma unroll
+    for (int h = 4; h >= 1; h >>= 1) {
+      const float o = __shfl_xor_sync(0xFFFFFFFFu, vmax, h, 8);
+      vmax = max_abs_nan(vmax, o);
+    }
+    if (!valid) continue;
+    const float amax = vmax != vmax ? __uint_as_float(0x7FC00000u) : vmax;
+    float s, r, unused;
+    block_scale_of<E5M2>(amax, &s, &r);
+    st_cs(y + row * cols + col, cast16<XT, E5M2>(raw, r, &unused));
+    if (l8 == 0) scales[row * ntc + tc] = s;
+  }
+}
+
+// 128 x 128 blocks: one CTA per block; thread t owns column segment t % 8 of
+// rows t / 8 + 32 k, k = 0..3, held in registers between the block amax and
+// the cast.
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(kThreads) void k_fp8_block_128x128(const void* __restrict__ x, int64_t rows,
+                                                                int64_t cols, uint8_t* __restrict__ y,
+                                                                float* __restrict__ scales) {
+  __shared__ uint32_t red[32];
+  __shared__ uint32_t amax_b;
+  const int64_t nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
+  const int cs = threadIdx.x & 7, rr = threadIdx.x >> 3;
+  for (int64_t b = blockIdx.x; b < nbr * nbc; b += gridDim.x) {
+    const int64_t br = b / nbc, bc = b % nbc;
+    const int64_t col = bc * 128 + cs * 16;
+    uint4 raw[4][4];
+    float vmax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t row = br * 128 + rr + 32 * k;
+      if (row < rows && col < cols) {
+        load_raw<XT>(x, (row * cols + col) / kElems, raw[k]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float2 f = pair_of<XT>(raw[k], j);
+          vmax = max_abs_nan(vmax, f.x);
+          vmax = max_abs_nan(vmax, f.y);
+        }
+      }
+    }
+    const uint32_t m = block_max_u32(amax_bits(vmax), red);
+    if (threadIdx.x == 0) amax_b = m;
+    __syncthreads();
+    float s, r, unused;
+    block_scale_of<E5M2>(__uint_as_float(amax_b), &s, &r);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t row = br * 128 + rr + 32 * k;
+      if (row < rows && col < cols) st_cs(y + row * cols + col, cast16<XT, E5M2>(raw[k], r, &unused));
+    }
+    if (threadIdx.x == 0) scales[br * nbc + bc] = s;
+    __syncthreads();  // red and amax_b are reused by the next block
+  }
+}
+
 template <typename K>
 int occ_of(K kernel) {
   int o = 0;
@@ -268,6 +373,23 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
   const int64_t tiles = ((rows + kTT - 1) / kTT) * ((cols + kTT - 1) / kTT);
   k_fp8_cast_t<XT, E5M2><<<grid_for(tiles, occ), kThreads, 0, s>>>(x, rows, cols, y, y_t, meta, hist, len, margin,
                                                                     algo);
+  note_launches(1);
+  return launch_status();
+}
+
+template <int XT, bool E5M2>
+mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool square, uint8_t* y, float* scales,
+                           cudaStream_t s) {
+  if (square) {
+    static const int occ = occ_of(k_fp8_block_128x128<XT, E5M2>);
+    const int64_t blocks = ((rows + 127) / 128) * ((cols + 127) / 128);
+    k_fp8_block_128x128<XT, E5M2><<<grid_for(blocks, occ), kThreads, 0, s>>>(x, rows, cols, y, scales);
+  } else {
+    static const int occ = occ_of(k_fp8_block_1x128<XT, E5M2>);
+    const int64_t quads = (rows * ((cols + 127) / 128) + 3) / 4;
+    const int64_t ctas = (quads + kThreads / 32 - 1) / (kThreads / 32);
+    k_fp8_block_1x128<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, rows, cols, y, scales);
+  }
   note_launches(1);
   return launch_status();
 }
@@ -336,5 +458,35 @@ extern "C" MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x
       return e5 ? launch_t<XBF16, true>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo, s)
                 : launch_t<XBF16, false>(x, rows, cols, yb, ytb, d_meta, d_history, history_len, margin, amax_algo,
                                          s);
+  }
+}
+
+extern "C" MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
+                                                   int32_t block_rows, int32_t block_cols, void* y,
+                                                   mp_dtype fp8_dtype, float* scales, void* stream) {
+  using namespace mp;
+  if (rows < 0 || cols < 0) return MP_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x || !y || !scales)) return MP_EINVAL;
+  if (x_dtype != MP_F32 && x_dtype != MP_F16 && x_dtype != MP_BF16) return MP_EINVAL;
+  if (fp8_dtype != MP_E4M3 && fp8_dtype != MP_E5M2) return MP_EINVAL;
+  const bool square = block_rows == 128 && block_cols == 128;
+  if (!square && !(block_rows == 1 && block_cols == 128)) return MP_ESHAPE;
+  if (cols % 16 != 0) return MP_ESHAPE;
+  if (n > 0 && (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(scales) & 3u))) return MP_EALIGN;
+  if (n == 0) return MP_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* yb = static_cast<uint8_t*>(y);
+  const bool e5 = fp8_dtype == MP_E5M2;
+  switch (x_dtype) {
+    case MP_F32:
+      return e5 ? launch_blockwise<XF32, true>(x, rows, cols, square, yb, scales, s)
+                : launch_blockwise<XF32, false>(x, rows, cols, square, yb, scales, s);
+    case MP_F16:
+      return e5 ? launch_blockwise<XF16, true>(x, rows, cols, square, yb, scales, s)
+                : launch_blockwise<XF16, false>(x, rows, cols, square, yb, scales, s);
+    default:
+      return e5 ? launch_blockwise<XBF16, true>(x, rows, cols, square, yb, scales, s)
+                : launch_blockwise<XBF16, false>(x, rows, cols, square, yb, scales, s);
   }
 }

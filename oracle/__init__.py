@@ -120,6 +120,7 @@ def lib() -> ctypes.CDLL:
             "orc_fp8_history_update": (None, [P, P, I32, F, F, ctypes.c_int, ctypes.c_int]),
             "orc_fp8_cast_delayed": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, P, P, I32, F, ctypes.c_int]),
             "orc_transpose_u8": (None, [P, I64, I64, P]),
+            "orc_fp8_quantize_blockwise": (None, [P, ctypes.c_int, I64, I64, I32, I32, ctypes.c_int, P, P]),
             "orc_nvfp4_prepare": (ctypes.c_int, [P, I64, I64, ctypes.c_int, U16, P]),
             "orc_nvfp4_tensor_scale": (F, [F, P]),
             "orc_nvfp4_encode_rows": (
@@ -267,6 +268,16 @@ def fp8_cast_delayed(x: np.ndarray, x_fmt: int, fmt: int, meta: Fp8Meta, history
         amax_algo
     )
     return y
+
+
+def fp8_quantize_blockwise(x: np.ndarray, x_fmt: int, block_rows: int, block_cols: int, fmt: int = E4M3):
+    """Returns (y [rows, cols] u8, scales [ceil(rows/br), ceil(cols/bc)] f32)."""
+    x = np.ascontiguousarray(x, dtype=_NP[x_fmt])
+    rows, cols = x.shape
+    y = np.empty((rows, cols), dtype=np.uint8)
+    sc = np.empty((-(-rows // block_rows), -(-cols // block_cols)), dtype=np.float32)
+    lib().orc_fp8_quantize_blockwise(_p(x), x_fmt, rows, cols, block_rows, block_cols, fmt, _p(y), _p(sc))
+    return y, sc
 
 
 def transpose_u8(y: np.ndarray) -> np.ndarray:

@@ -479,6 +479,33 @@ void orc_transpose_u8(const uint8_t* y, int64_t rows, int64_t cols, uint8_t* y_t
     for (int64_t c = 0; c < cols; ++c) y_t[c * rows + r] = y[r * cols + c];
 }
 
+void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t cols, int32_t block_rows,
+                                int32_t block_cols, int fmt, uint8_t* y, float* scales) {
+  float fp8_max = (fmt == ORC_E4M3) ? 448.0f : 57344.0f;
+  int64_t nbr = (rows + block_rows - 1) / block_rows, nbc = (cols + block_cols - 1) / block_cols;
+  for (int64_t br = 0; br < nbr; ++br) {
+    for (int64_t bc = 0; bc < nbc; ++bc) {
+      int64_t r1 = (br + 1) * block_rows < rows ? (br + 1) * block_rows : rows;
+      int64_t c1 = (bc + 1) * block_cols < cols ? (bc + 1) * block_cols : cols;
+      float amax = 0.0f;
+      int nan = 0;
+      for (int64_t r = br * block_rows; r < r1; ++r)
+        for (int64_t c = bc * block_cols; c < c1; ++c) {
+          float a = fabsf(load_f32(x, x_fmt, r * cols + c));
+          if (isnan(a)) nan = 1;
+          else if (a > amax) amax = a;
+        }
+      if (nan) amax = u2f(0x7FC00000u);
+      /* a block holding a NaN stores the quiet NaN 0x7FC00000 as its scale */
+      scales[br * nbc + bc] = nan ? amax : amax / fp8_max;
+      float rr = (isfinite(amax) && amax > 0.0f) ? fp8_max / amax : 0.0f;
+      for (int64_t r = br * block_rows; r < r1; ++r)
+        for (int64_t c = bc * block_cols; c < c1; ++c)
+          y[r * cols + c] = orc_f32_to_fp8_sat(load_f32(x, x_fmt, r * cols + c) * rr, fmt);
+    }
+  }
+}
+
 /* ---------------------------------------------------------------------------
  * NVFP4 ([NVFP4] §2.1 "NVFP4 포맷의 특징", §2.2): 16-element blocks, one E4M3
  * block scale per block under one FP32 tensor scale (two-level scaling);

@@ -155,6 +155,17 @@ void orc_fp8_cast_delayed(const void* x, int x_fmt, int64_t n, uint8_t* y, int f
 /* y_t[c][r] = y[r][c] for a [rows][cols] byte matrix. */
 void orc_transpose_u8(const uint8_t* y, int64_t rows, int64_t cols, uint8_t* y_t);
 
+/* ---- fine-grained FP8 with online block scales ([MPT-ko] "FP8 혼합 정밀도";
+ * [FP8-TE] "DeepSeek-V3 FP8 학습 사례"): activations in 1x128 tiles, weights in
+ * 128x128 blocks, each block's scale computed from the block itself (no
+ * history).  Reading R20: amax = max |x| over the block; the stored scale is
+ * s = amax / fp8_max (the quiet NaN 0x7FC00000 for a block holding a NaN);
+ * elements are y = sat(RNE(fp32(x) * r)) with
+ * r = fp8_max / amax when amax is finite and > 0, else r = 0.  Blocks at the
+ * right and bottom edges may be partial.  scales: [ceil(rows/br)][ceil(cols/bc)]. */
+void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t cols, int32_t block_rows,
+                                int32_t block_cols, int fmt, uint8_t* y, float* scales);
+
 /* ---- NVFP4 quantisation ([NVFP4] §2.1, §2.2) ---------------------------------- */
 /* x' = x or RHT(x), as FP32. */
 int orc_nvfp4_prepare(const uint16_t* x_bf16, int64_t rows, int64_t cols, int apply_rht,
