@@ -121,6 +121,7 @@ def lib() -> ctypes.CDLL:
             "orc_fp8_cast_delayed": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, P, P, I32, F, ctypes.c_int]),
             "orc_transpose_u8": (None, [P, I64, I64, P]),
             "orc_fp8_quantize_blockwise": (None, [P, ctypes.c_int, I64, I64, I32, I32, ctypes.c_int, P, P]),
+            "orc_mx_quantize": (None, [P, ctypes.c_int, I64, I64, ctypes.c_int, P, P, P]),
             "orc_nvfp4_prepare": (ctypes.c_int, [P, I64, I64, ctypes.c_int, U16, P]),
             "orc_nvfp4_tensor_scale": (F, [F, P]),
             "orc_nvfp4_encode_rows": (
@@ -278,6 +279,17 @@ def fp8_quantize_blockwise(x: np.ndarray, x_fmt: int, block_rows: int, block_col
     sc = np.empty((-(-rows // block_rows), -(-cols // block_cols)), dtype=np.float32)
     lib().orc_fp8_quantize_blockwise(_p(x), x_fmt, rows, cols, block_rows, block_cols, fmt, _p(y), _p(sc))
     return y, sc
+
+
+def mx_quantize(x: np.ndarray, x_fmt: int, elem_fmt: int, want_dequant: bool = True):
+    """Returns (codes, scales [rows, cols/32] u8 UE8M0, dequant u16 | None)."""
+    x = np.ascontiguousarray(x, dtype=_NP[x_fmt])
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2 if elem_fmt == E2M1 else cols), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    dq = np.zeros((rows, cols), dtype=np.uint16) if want_dequant else None
+    lib().orc_mx_quantize(_p(x), x_fmt, rows, cols, elem_fmt, _p(codes), _p(scales), _p(dq))
+    return codes, scales, dq
 
 
 def transpose_u8(y: np.ndarray) -> np.ndarray:

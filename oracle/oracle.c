@@ -506,6 +506,55 @@ void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t 
   }
 }
 
+void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int elem_fmt, uint8_t* codes,
+                     uint8_t* scales, uint16_t* dequant) {
+  int emax = elem_fmt == ORC_E4M3 ? 8 : (elem_fmt == ORC_E5M2 ? 15 : 2);
+  int64_t nb = cols / 32;
+  for (int64_t r = 0; r < rows; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      int64_t base = r * cols + b * 32;
+      float amax = 0.0f;
+      int bad = 0;
+      for (int j = 0; j < 32; ++j) {
+        float a = fabsf(load_f32(x, x_fmt, base + j));
+        if (!isfinite(a)) bad = 1;
+        else if (a > amax) amax = a;
+      }
+      int e = -127;
+      if (!bad && amax > 0.0f) {
+        int k;
+        frexp((double)amax, &k); /* amax = f * 2^k, f in [0.5, 1) */
+        e = (k - 1) - emax;
+        if (e < -127) e = -127;
+        if (e > 127) e = 127;
+      }
+      scales[r * nb + b] = bad ? 0xFF : (uint8_t)(e + 127);
+      float mul = (float)ldexp(1.0, -e); /* 2^-e, exact in binary32 for e in [-127, 127] */
+      double dq = ldexp(1.0, e);
+      for (int j = 0; j < 32; ++j) {
+        int64_t i = base + j;
+        uint8_t q = 0;
+        if (!bad) {
+          float y = load_f32(x, x_fmt, i) * mul;
+          q = (elem_fmt == ORC_E2M1) ? orc_f32_to_e2m1(y) : orc_f32_to_fp8_sat(y, elem_fmt);
+        }
+        if (elem_fmt == ORC_E2M1) {
+          uint8_t* byte = &codes[i >> 1];
+          if (i & 1) *byte = (uint8_t)((*byte & 0x0F) | (q << 4));
+          else *byte = (uint8_t)((*byte & 0xF0) | q);
+        } else {
+          codes[i] = q;
+        }
+        if (dequant) {
+          float v = bad ? 0.0f
+                        : (elem_fmt == ORC_E2M1 ? orc_e2m1_to_f32(q) : orc_fp8_to_f32(q, elem_fmt)) * (float)dq;
+          dequant[i] = orc_f32_to_bf16(v);
+        }
+      }
+    }
+  }
+}
+
 /* ---------------------------------------------------------------------------
  * NVFP4 ([NVFP4] §2.1 "NVFP4 포맷의 특징", §2.2): 16-element blocks, one E4M3
  * block scale per block under one FP32 tensor scale (two-level scaling);

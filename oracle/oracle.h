@@ -166,6 +166,20 @@ void orc_transpose_u8(const uint8_t* y, int64_t rows, int64_t cols, uint8_t* y_t
 void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t cols, int32_t block_rows,
                                 int32_t block_cols, int fmt, uint8_t* y, float* scales);
 
+/* ---- MX block formats ([MPT-ko] "FP8 혼합 정밀도": MXFP8 / MXFP6 / MXFP4, one
+ * power-of-two scale per 32 elements; [NVFP4] §2.1: MXFP4 = 32-element blocks
+ * with a UE8M0 scale).  Reading R21: for a block of 32 elements along a row,
+ * e = floor(log2(amax)) - emax_elem (emax_elem = 8, 15, 2 for E4M3, E5M2,
+ * E2M1: the exponent of the format's largest value), clamped to
+ * [-127, 127]; amax = 0 gives e = -127.  The scale byte is e + 127 (UE8M0);
+ * elements are RNE(fp32(x) * 2^-e) saturating to the element format.  A
+ * non-finite amax gives the scale byte 0xFF and all element codes 0.
+ * codes: 1 byte per element (E4M3/E5M2) or two E2M1 codes per byte, element
+ * 2j in the low nibble; scales [rows][cols / 32]; dequant (optional) is
+ * BF16 RNE of value(code) * 2^e. */
+void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int elem_fmt, uint8_t* codes,
+                     uint8_t* scales, uint16_t* dequant);
+
 /* ---- NVFP4 quantisation ([NVFP4] §2.1, §2.2) ---------------------------------- */
 /* x' = x or RHT(x), as FP32. */
 int orc_nvfp4_prepare(const uint16_t* x_bf16, int64_t rows, int64_t cols, int apply_rht,
