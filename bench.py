@@ -244,6 +244,7 @@ class Workload:
 
         r, g4 = W.NVFP4_RNE, W.NVFP4_GRAD
         self.q = []
+        self.extra_bytes = {}
         for name, rows, cols, rec, b2, sr, rht, seed, mask in (
             ("nvfp4_act_1x16_rne", r.act_rows, r.act_cols, r.act_recipe(), False, False, False, 0, 0),
             ("nvfp4_w_16x16_rne", r.w_rows, r.w_cols, r.w_recipe(), True, False, False, 0, 0),
@@ -317,11 +318,31 @@ class Workload:
             "fp8_grad_e5m2": lambda k: M.fp8_cast_delayed(self.grd[k % self.nbuf], self.y_grd, M.MP_E5M2,
                                                           self.meta_grd, self.hist_grd, self.fp8_margin),
         }
+        # calls outside the step, each with its algorithmic bytes per call
         f = self.fp8_rows_cols
-        yt = torch.empty(self.fp8_n, dtype=torch.uint8, device="cuda")
+        n_fp8 = self.fp8_n
+        yt = torch.empty(n_fp8, dtype=torch.uint8, device="cuda")
         calls["fp8_act_e4m3_with_transpose"] = lambda k: M.fp8_cast_transpose_delayed(
             self.act[k % self.nbuf].view(*f), self.y_act, yt, M.MP_E4M3, self.meta_act, self.hist_act,
             self.fp8_margin)
+        self.extra_bytes["fp8_act_e4m3_with_transpose"] = (B_FP8 + 1.0) * n_fp8  # read 2, write y 1 and y_t 1
+        sc128 = torch.empty(f[0] * (f[1] // 128), dtype=torch.float32, device="cuda")
+        calls["fp8_blockwise_1x128_act"] = lambda k: M.fp8_quantize_blockwise(
+            self.act[k % self.nbuf].view(*f), self.y_act, sc128, 1, 128)
+        self.extra_bytes["fp8_blockwise_1x128_act"] = (3.0 + 4.0 / 128) * n_fp8
+        wq = self.q[1]
+        yw = torch.empty(wq["rows"] * wq["cols"], dtype=torch.uint8, device="cuda")
+        scw = torch.empty(-(-wq["rows"] // 128) * -(-wq["cols"] // 128), dtype=torch.float32, device="cuda")
+        calls["fp8_blockwise_128x128_w"] = lambda k: M.fp8_quantize_blockwise(wq["x"], yw, scw, 128, 128)
+        self.extra_bytes["fp8_blockwise_128x128_w"] = (3.0 + 4.0 / 16384) * wq["rows"] * wq["cols"]
+        aq = self.q[0]
+        n_a = aq["rows"] * aq["cols"]
+        mx_c = torch.empty(n_a, dtype=torch.uint8, device="cuda")
+        mx_s = torch.empty(n_a // 32, dtype=torch.uint8, device="cuda")
+        calls["mxfp4_act"] = lambda k: M.mx_quantize(aq["x"], mx_c, mx_s, M.MP_E2M1)
+        self.extra_bytes["mxfp4_act"] = (2.5 + 1.0 / 32) * n_a
+        calls["mxfp8_e4m3_act"] = lambda k: M.mx_quantize(aq["x"], mx_c, mx_s, M.MP_E4M3)
+        self.extra_bytes["mxfp8_e4m3_act"] = (3.0 + 1.0 / 32) * n_a
         for q in self.q:
             calls[q["name"]] = (lambda q: lambda k: M.nvfp4_quantize(
                 q["x"], q["codes"], q["scales"], q["ts"], q["nf"], q["ws"], block_2d=q["b2"], stochastic=q["sr"],
@@ -601,10 +622,10 @@ def main():
     # Each quantiser call alone: 16 back-to-back calls captured in a CUDA
     # graph and replayed after an L2-clean point, so neither launch gaps nor
     # the previous kernel's dirty L2 lines are charged to it.
-    isolated = wl.isolated_call_times() if not args.small else {}
+    isolated = wl.isolated_call_times(reps=2 if args.small else 16)
     for name, us in isolated.items():
         if name not in kernels:  # calls measured only in isolation
-            wl.bytes[name] = (B_FP8 + 1.0) * wl.fp8_n  # read 2, write y 1 and y_t 1
+            wl.bytes[name] = wl.extra_bytes[name]
             kernels[name] = {"bytes": int(wl.bytes[name]), "note": "not in the step; graph-replayed only"}
         gbs = wl.bytes[name] / (us * 1e-6) / 1e9
         kernels[name]["graph_isolated_us"] = round(us, 2)

@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmpnum.so")
 
 MP_OK, MP_EINVAL, MP_EALIGN, MP_ESHAPE, MP_EWORKSPACE, MP_ECUDA = 0, -1, -2, -3, -4, -5
-MP_F32, MP_F16, MP_BF16, MP_E4M3, MP_E5M2 = 0, 1, 2, 3, 4
+MP_F32, MP_F16, MP_BF16, MP_E4M3, MP_E5M2, MP_E2M1 = 0, 1, 2, 3, 4, 5
 
 
 class MpParam(ctypes.Structure):
@@ -108,6 +108,7 @@ def _load() -> ctypes.CDLL:
         "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
         "nvfp4_noalloc_scratch_bytes": (S, []),
         "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P]),
+        "mx_quantize": (I32, [P, I32, I64, I64, I32, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)
@@ -343,9 +344,17 @@ def rht16(x, y, sign_mask: int, stream=None) -> None:
     _check("rht16", lib.rht16(_ptr(x), rows, cols, sign_mask & 0xFFFF, _ptr(y), _dtype_code(y), _stream(stream)))
 
 
+def mx_quantize(x, codes, scales, elem_dtype: int = MP_E2M1, dequant=None, stream=None) -> None:
+    """x: [rows, cols], cols % 32 == 0; codes: rows*cols bytes (FP8) or
+    rows*cols/2 (E2M1); scales: uint8 [rows, cols/32] (UE8M0)."""
+    rows, cols = x.shape
+    _check("mx_quantize", lib.mx_quantize(_ptr(x), _dtype_code(x), rows, cols, elem_dtype, _ptr(codes),
+                                          _ptr(scales), _ptr(dequant), _stream(stream)))
+
+
 __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
-    "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2",
+    "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2", "MP_E2M1", "mx_quantize",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
     "fp8_cast_transpose_delayed", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",

@@ -13,7 +13,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmpnum.so")
 HEADER = os.path.join(ROOT, "include", "mpnum.h")
 
-SOURCES = ["mp_common.cu", "mp_adamw.cu", "mp_fp8.cu", "mp_nvfp4.cu"]
+SOURCES = ["mp_common.cu", "mp_adamw.cu", "mp_fp8.cu", "mp_nvfp4.cu", "mp_mx.cu"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = GENCODE + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                         "-I", os.path.join(ROOT, "include")]

@@ -91,6 +91,14 @@ def test_argument_validation_without_gpu(M):
     assert q(8, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_EALIGN
     assert L.rht16(16, 2, 40, 0, 16, M.MP_F32, None) == M.MP_ESHAPE
     assert L.rht16(16, 2, 32, 0, 16, M.MP_E4M3, None) == M.MP_EINVAL
+    mx = L.mx_quantize
+    assert mx(16, M.MP_BF16, 2, 48, M.MP_E4M3, 16, 16, None, None) == M.MP_ESHAPE
+    assert mx(16, M.MP_BF16, 2, 64, M.MP_F16, 16, 16, None, None) == M.MP_EINVAL
+    assert mx(16, M.MP_E4M3, 2, 64, M.MP_E2M1, 16, 16, None, None) == M.MP_EINVAL
+    assert mx(16, M.MP_BF16, 2, 64, M.MP_E2M1, 8, 16, None, None) == M.MP_EALIGN
+    assert mx(16, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, 40, None) == M.MP_EALIGN
+    assert mx(None, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, None, None) == M.MP_EINVAL
+    assert mx(None, M.MP_BF16, 0, 64, M.MP_E2M1, None, None, None, None) == M.MP_OK
     assert M.mp_launch_count() == 0
 
 
