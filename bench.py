@@ -310,43 +310,63 @@ class Workload:
         return statistics.median(ev[2 * k].elapsed_time(ev[2 * k + 1]) for k in range(reps))
 
     def isolated_call_times(self, reps: int = 16) -> dict:
-        """Microseconds per call of each FP8 / NVFP4 call, replayed from a CUDA graph."""
+        """Microseconds per call of each FP8 / NVFP4 / MX call, replayed from a
+        CUDA graph.  Consecutive calls read different copies of their input and
+        write different copies of their outputs (each set more than twice the
+        L2), so no call finds its input in L2 and no output is rewritten while
+        its lines still sit dirty in L2."""
         torch, M = self.torch, self.M
+        l2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+
+        def rot(x, clone=True):
+            nbytes = x.numel() * x.element_size()
+            n = 1 if nbytes < (4 << 20) else min(reps, max(1, -(-2 * l2 // nbytes)))
+            return [x] + [x.clone() if clone else torch.empty_like(x) for _ in range(n - 1)]
+
+        def pick(lst, k):
+            return lst[k % len(lst)]
+
+        xs = {q["name"]: rot(q["x"]) for q in self.q}
+        f = self.fp8_rows_cols
+        n_fp8 = self.fp8_n
+        y8 = rot(self.y_act, clone=False)
+        y8g = rot(self.y_grd, clone=False)
         calls = {
-            "fp8_act_e4m3": lambda k: M.fp8_cast_delayed(self.act[k % self.nbuf], self.y_act, M.MP_E4M3,
+            "fp8_act_e4m3": lambda k: M.fp8_cast_delayed(self.act[k % self.nbuf], pick(y8, k), M.MP_E4M3,
                                                          self.meta_act, self.hist_act, self.fp8_margin),
-            "fp8_grad_e5m2": lambda k: M.fp8_cast_delayed(self.grd[k % self.nbuf], self.y_grd, M.MP_E5M2,
+            "fp8_grad_e5m2": lambda k: M.fp8_cast_delayed(self.grd[k % self.nbuf], pick(y8g, k), M.MP_E5M2,
                                                           self.meta_grd, self.hist_grd, self.fp8_margin),
         }
         # calls outside the step, each with its algorithmic bytes per call
-        f = self.fp8_rows_cols
-        n_fp8 = self.fp8_n
-        yt = torch.empty(n_fp8, dtype=torch.uint8, device="cuda")
+        yt = rot(torch.empty(n_fp8, dtype=torch.uint8, device="cuda"), clone=False)
         calls["fp8_act_e4m3_with_transpose"] = lambda k: M.fp8_cast_transpose_delayed(
-            self.act[k % self.nbuf].view(*f), self.y_act, yt, M.MP_E4M3, self.meta_act, self.hist_act,
+            self.act[k % self.nbuf].view(*f), pick(y8, k), pick(yt, k), M.MP_E4M3, self.meta_act, self.hist_act,
             self.fp8_margin)
         self.extra_bytes["fp8_act_e4m3_with_transpose"] = (B_FP8 + 1.0) * n_fp8  # read 2, write y 1 and y_t 1
         sc128 = torch.empty(f[0] * (f[1] // 128), dtype=torch.float32, device="cuda")
         calls["fp8_blockwise_1x128_act"] = lambda k: M.fp8_quantize_blockwise(
-            self.act[k % self.nbuf].view(*f), self.y_act, sc128, 1, 128)
+            self.act[k % self.nbuf].view(*f), pick(y8, k), sc128, 1, 128)
         self.extra_bytes["fp8_blockwise_1x128_act"] = (3.0 + 4.0 / 128) * n_fp8
         wq = self.q[1]
-        yw = torch.empty(wq["rows"] * wq["cols"], dtype=torch.uint8, device="cuda")
+        wr = xs[wq["name"]]
+        yw = rot(torch.empty(wq["rows"] * wq["cols"], dtype=torch.uint8, device="cuda"), clone=False)
         scw = torch.empty(-(-wq["rows"] // 128) * -(-wq["cols"] // 128), dtype=torch.float32, device="cuda")
-        calls["fp8_blockwise_128x128_w"] = lambda k: M.fp8_quantize_blockwise(wq["x"], yw, scw, 128, 128)
+        calls["fp8_blockwise_128x128_w"] = lambda k: M.fp8_quantize_blockwise(pick(wr, k), pick(yw, k), scw, 128, 128)
         self.extra_bytes["fp8_blockwise_128x128_w"] = (3.0 + 4.0 / 16384) * wq["rows"] * wq["cols"]
         aq = self.q[0]
         n_a = aq["rows"] * aq["cols"]
-        mx_c = torch.empty(n_a, dtype=torch.uint8, device="cuda")
-        mx_s = torch.empty(n_a // 32, dtype=torch.uint8, device="cuda")
-        calls["mxfp4_act"] = lambda k: M.mx_quantize(aq["x"], mx_c, mx_s, M.MP_E2M1)
+        ar = xs[aq["name"]]
+        mx_c = rot(torch.empty(n_a, dtype=torch.uint8, device="cuda"), clone=False)
+        mx_s = rot(torch.empty(n_a // 32, dtype=torch.uint8, device="cuda"), clone=False)
+        calls["mxfp4_act"] = lambda k: M.mx_quantize(pick(ar, k), pick(mx_c, k)[: n_a // 2], pick(mx_s, k), M.MP_E2M1)
         self.extra_bytes["mxfp4_act"] = (2.5 + 1.0 / 32) * n_a
-        calls["mxfp8_e4m3_act"] = lambda k: M.mx_quantize(aq["x"], mx_c, mx_s, M.MP_E4M3)
+        calls["mxfp8_e4m3_act"] = lambda k: M.mx_quantize(pick(ar, k), pick(mx_c, k), pick(mx_s, k), M.MP_E4M3)
         self.extra_bytes["mxfp8_e4m3_act"] = (3.0 + 1.0 / 32) * n_a
         for q in self.q:
-            calls[q["name"]] = (lambda q: lambda k: M.nvfp4_quantize(
-                q["x"], q["codes"], q["scales"], q["ts"], q["nf"], q["ws"], block_2d=q["b2"], stochastic=q["sr"],
-                seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"]))(q)
+            qc, qs = rot(q["codes"], clone=False), rot(q["scales"], clone=False)
+            calls[q["name"]] = (lambda q, xr, qc, qs: lambda k: M.nvfp4_quantize(
+                pick(xr, k), pick(qc, k), pick(qs, k), q["ts"], q["nf"], q["ws"], block_2d=q["b2"],
+                stochastic=q["sr"], seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"]))(q, xs[q["name"]], qc, qs)
         clean = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
         out = {}
         for name, fn in calls.items():

@@ -145,7 +145,7 @@ MP_API void mp_scaler_state_init(mp_scaler_state* host_state, float init_scale);
  * d_state->clip_coef ([MPT-ko] "FP16 학습 루프"; [MPT-es] "Operaciones que
  * permanecen en FP32": gradient norms are long reductions kept in FP32).
  * Clipping needs d_workspace of mp_adamw_workspace_size(params, n_params)
- * bytes (device, 4-byte aligned, any contents); without clipping it may be
+ * bytes (device, 8-byte aligned, any contents); without clipping it may be
  * NULL.
  * The host array `params` (n_params >= 0 entries) is read during the call
  * only; its pointers are device pointers, 16-byte aligned.  grad_dtype and

@@ -120,36 +120,65 @@ __device__ __forceinline__ float g_lo(uint32_t w) { return BF16 ? bf16lo(w) : f1
 template <bool BF16>
 __device__ __forceinline__ float g_hi(uint32_t w) { return BF16 ? bf16hi(w) : f16hi(w); }
 
+constexpr int kClipCtasPerSm = 4;  // register cap of the clipping check pass: 4 x 32 KB tiles in flight per SM
+
+// Thread 0: fold the 8 warp sums of a tile as w[i] += w[i + h], h = 4, 2, 1.
+__device__ __forceinline__ float fold_warp_sums(const float* ws) {
+  float w[kThreads / 32];
+#pragma unroll
+  for (int i = 0; i < kThreads / 32; ++i) w[i] = ws[i];
+#pragma unroll
+  for (int h = kThreads / 64; h >= 1; h >>= 1)
+#pragma unroll
+    for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[i], w[i + h]);
+  return w[0];
+}
+
 // With CLIP, every tile of kTile elements also yields the binary32 sum of
 // g*g, g = fp32(grad) * inv_scale, in one fixed order: lane t sums its 8
 // vectors (u = 0..7) element by element; each warp folds its 32 lane sums by
 // v[l] += v[l ^ h], h = 16..1; the 8 warp sums fold as w[i] += w[i + h],
-// h = 4, 2, 1.  The sum goes to tile_sums[tile_base + tile].
+// h = 4, 2, 1.  The sum goes to tile_sums[tile_base + tile].  The warp sums of
+// a tile are folded one iteration later, after the next tile's loads are in
+// flight, so the CTA's one barrier per tile never holds back a load.
 template <int CAP, bool GBF16, bool CLIP>
-__global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant__ Table<CAP> T,
-                                                           mp_scaler_state* st,
-                                                           const mp_adamw_hparams hp, int finalize,
-                                                           float* __restrict__ tile_sums, int64_t tile_base) {
-  __shared__ float warp_sum[kThreads / 32];
+__device__ __forceinline__ void check_body(const Table<CAP>& T, mp_scaler_state* st, const mp_adamw_hparams& hp,
+                                           int finalize, float* __restrict__ tile_sums, int64_t tile_base) {
+  __shared__ float warp_sum[2][kThreads / 32];
   uint32_t bad = 0;
   const float inv_scale = CLIP ? __double2float_rn(__ddiv_rn(1.0, (double)st->scale)) : 0.0f;
   const int64_t total = T.tile_start[T.count];
+  int par = 0;
+  int64_t prev = -1;  // tile whose warp sums wait in warp_sum[par ^ 1]
   for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
     const int ti = find_tensor(T, tile);
     const TensorDesc& d = T.t[ti];
     const int64_t base = (tile - T.tile_start[ti]) * kTile;
+    const bool whole = base + kTile <= d.n;  // every vector of the tile is in the tensor
     uint4 g[kUnroll];
-    bool full[kUnroll];
+    if (whole) {
+      const uint4* gp = reinterpret_cast<const uint4*>(d.g + base) + threadIdx.x;
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int64_t e = base + ((int64_t)u * kThreads + threadIdx.x) * kVec;
-      full[u] = e + kVec <= d.n;
-      if (full[u]) g[u] = ld_cs(d.g + e);
+      for (int u = 0; u < kUnroll; ++u) g[u] = __ldcs(gp + u * kThreads);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t e = base + ((int64_t)u * kThreads + threadIdx.x) * kVec;
+        if (e + kVec <= d.n) g[u] = ld_cs(d.g + e);
+      }
+    }
+    if (CLIP) {
+      // Every warp wrote its sums of tile `prev` before issuing this tile's
+      // loads; thread 0 reads them before it reaches the next barrier, so the
+      // slot is free again when it is rewritten two tiles later.
+      __syncthreads();
+      if (threadIdx.x == 0 && prev >= 0) tile_sums[tile_base + prev] = fold_warp_sums(warp_sum[par ^ 1]);
     }
     float lane = 0.0f;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if (full[u]) {
+      const int64_t e = base + ((int64_t)u * kThreads + threadIdx.x) * kVec;
+      if (whole || e + kVec <= d.n) {
         bad |= nonfinite_bits<GBF16>(g[u].x) | nonfinite_bits<GBF16>(g[u].y) |
                nonfinite_bits<GBF16>(g[u].z) | nonfinite_bits<GBF16>(g[u].w);
         if (CLIP) {
@@ -163,7 +192,6 @@ __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant
           }
         }
       } else {
-        const int64_t e = base + ((int64_t)u * kThreads + threadIdx.x) * kVec;
         for (int64_t i = e; i < d.n; ++i) {
           const uint32_t h = d.g[i];
           bad |= nonfinite_bits<GBF16>(h) & 0x8000u;
@@ -177,20 +205,14 @@ __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant
     if (CLIP) {
 #pragma unroll
       for (int h = 16; h >= 1; h >>= 1) lane = __fadd_rn(lane, __shfl_xor_sync(0xFFFFFFFFu, lane, h));
-      if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = lane;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        float w[kThreads / 32];
-#pragma unroll
-        for (int i = 0; i < kThreads / 32; ++i) w[i] = warp_sum[i];
-#pragma unroll
-        for (int h = kThreads / 64; h >= 1; h >>= 1)
-#pragma unroll
-          for (int i = 0; i < h; ++i) w[i] = __fadd_rn(w[i], w[i + h]);
-        tile_sums[tile_base + tile] = w[0];
-      }
-      __syncthreads();  // warp_sum is rewritten by the next tile
+      if ((threadIdx.x & 31) == 0) warp_sum[par][threadIdx.x >> 5] = lane;
+      prev = tile;
+      par ^= 1;
     }
+  }
+  if (CLIP) {
+    __syncthreads();
+    if (threadIdx.x == 0 && prev >= 0) tile_sums[tile_base + prev] = fold_warp_sums(warp_sum[par ^ 1]);
   }
   const int any = __syncthreads_or((bad & 0x80008000u) != 0);
   if (threadIdx.x == 0) {
@@ -208,34 +230,68 @@ __global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant
   }
 }
 
-// Folds the tile sums in binary64 in one fixed order (lane t of 1024 adds
-// tiles t, t + 1024, ...; each warp folds by v[l] += v[l ^ h], h = 16..1; the
-// 32 warp sums fold as w[i] += w[i + h], h = 16..1), then
-// norm = sqrt(total) and clip = min(1, max_norm / (norm + 1e-6)).
-constexpr int kFinishThreads = 1024;
-__global__ __launch_bounds__(kFinishThreads) void k_clip_finish(const float* __restrict__ tile_sums, int64_t ntiles,
-                                                                mp_scaler_state* st, float max_norm) {
-  __shared__ double warp_sum[kFinishThreads / 32];
+template <int CAP, bool GBF16>
+__global__ __launch_bounds__(kThreads) void k_check_finite(const __grid_constant__ Table<CAP> T, mp_scaler_state* st,
+                                                           const mp_adamw_hparams hp, int finalize) {
+  check_body<CAP, GBF16, false>(T, st, hp, finalize, nullptr, 0);
+}
+
+template <int CAP, bool GBF16>
+__global__ __launch_bounds__(kThreads, kClipCtasPerSm) void k_check_finite_clip(
+    const __grid_constant__ Table<CAP> T, mp_scaler_state* st, const mp_adamw_hparams hp, int finalize,
+    float* __restrict__ tile_sums, int64_t tile_base) {
+  check_body<CAP, GBF16, true>(T, st, hp, finalize, tile_sums, tile_base);
+}
+
+// Folds the tile sums in binary64 in one fixed order: lane t of kFoldLanes
+// adds tiles t, t + kFoldLanes, t + 2 kFoldLanes, ... in that order; each warp
+// folds its lanes by v[l] += v[l ^ h], h = 16..1; the warp sums fold as
+// w[i] += w[i + h], h = 16..1; then norm = sqrt(total) and
+// clip = min(1, max_norm / (norm + 1e-6)).  One warp per CTA, one CTA per
+// warp of lanes, so the binary64 additions spread over 32 SMs; loads are
+// batched kFoldBatch deep and added in lane order.  The last CTA (atomic
+// ticket on st->internal_ticket, which the check pass leaves at zero; no
+// waiting) folds the warp sums.
+constexpr int kFoldLanes = 1024;
+constexpr int kFoldCtas = kFoldLanes / 32;
+constexpr int kFoldBatch = 32;
+constexpr size_t kFoldBytes = kFoldCtas * sizeof(double);  // warp sums at the start of the workspace
+__global__ __launch_bounds__(32) void k_clip_finish(const float* __restrict__ tile_sums, int64_t ntiles,
+                                                    double* __restrict__ warp_sums, mp_scaler_state* st,
+                                                    float max_norm) {
+  const int64_t t = (int64_t)blockIdx.x * 32 + threadIdx.x;
   double lane = 0.0;
-  for (int64_t i = threadIdx.x; i < ntiles; i += kFinishThreads) lane = __dadd_rn(lane, (double)tile_sums[i]);
+  for (int64_t i0 = t; i0 < ntiles; i0 += (int64_t)kFoldLanes * kFoldBatch) {
+    float v[kFoldBatch];
+#pragma unroll
+    for (int j = 0; j < kFoldBatch; ++j) {
+      const int64_t i = i0 + (int64_t)j * kFoldLanes;
+      v[j] = i < ntiles ? __ldcg(tile_sums + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < kFoldBatch; ++j)
+      if (i0 + (int64_t)j * kFoldLanes < ntiles) lane = __dadd_rn(lane, (double)v[j]);
+  }
 #pragma unroll
   for (int h = 16; h >= 1; h >>= 1) lane = __dadd_rn(lane, __shfl_xor_sync(0xFFFFFFFFu, lane, h));
-  if ((threadIdx.x & 31) == 0) warp_sum[threadIdx.x >> 5] = lane;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double w[kFinishThreads / 32];
+  if (threadIdx.x != 0) return;
+  warp_sums[blockIdx.x] = lane;
+  __threadfence();
+  if (atomicAdd(&st->internal_ticket, 1u) != gridDim.x - 1) return;
+  __threadfence();
+  st->internal_ticket = 0;
+  double w[kFoldCtas];
 #pragma unroll
-    for (int i = 0; i < kFinishThreads / 32; ++i) w[i] = warp_sum[i];
+  for (int i = 0; i < kFoldCtas; ++i) w[i] = __ldcg(warp_sums + i);
 #pragma unroll
-    for (int h = kFinishThreads / 64; h >= 1; h >>= 1)
+  for (int h = kFoldCtas / 2; h >= 1; h >>= 1)
 #pragma unroll
-      for (int i = 0; i < h; ++i) w[i] = __dadd_rn(w[i], w[i + h]);
-    const double norm = __dsqrt_rn(w[0]);
-    double c = __ddiv_rn((double)max_norm, __dadd_rn(norm, 1e-6));
-    if (c > 1.0) c = 1.0;
-    st->grad_norm = __double2float_rn(norm);
-    st->clip_coef = __double2float_rn(c);
-  }
+    for (int i = 0; i < h; ++i) w[i] = __dadd_rn(w[i], w[i + h]);
+  const double norm = __dsqrt_rn(w[0]);
+  double c = __ddiv_rn((double)max_norm, __dadd_rn(norm, 1e-6));
+  if (c > 1.0) c = 1.0;
+  st->grad_norm = __double2float_rn(norm);
+  st->clip_coef = __double2float_rn(c);
 }
 
 struct Scalars {
@@ -419,7 +475,8 @@ void fill_table(Table<CAP>& T, const mp_param* const* list, int count, int64_t t
 
 struct ClipArgs {
   bool on;
-  float* tile_sums;
+  double* warp_sums;  // kFoldCtas binary64 partial sums (start of the workspace)
+  float* tile_sums;   // one binary32 sum per tile (after them)
   float max_norm;
 };
 
@@ -432,13 +489,13 @@ mp_status launch_group(const mp_param* const* list, int count, bool finalize, bo
     fill_table(Tl, list, count, kTile);
     *tiles_out = Tl.tile_start[count];
     if (clip.on) {
-      static const int occ = occupancy(k_check_finite<CAP, GBF16, true>, kThreads, 0);
-      k_check_finite<CAP, GBF16, true><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(
+      static const int occ = occupancy(k_check_finite_clip<CAP, GBF16>, kThreads, 0);
+      k_check_finite_clip<CAP, GBF16><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(
           Tl, st, hp, finalize ? 1 : 0, clip.tile_sums, tile_base);
     } else {
-      static const int occ = occupancy(k_check_finite<CAP, GBF16, false>, kThreads, 0);
-      k_check_finite<CAP, GBF16, false><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(
-          Tl, st, hp, finalize ? 1 : 0, nullptr, 0);
+      static const int occ = occupancy(k_check_finite<CAP, GBF16>, kThreads, 0);
+      k_check_finite<CAP, GBF16><<<grid_for(Tl.tile_start[count], occ), kThreads, 0, s>>>(Tl, st, hp,
+                                                                                           finalize ? 1 : 0);
     }
   } else {
     fill_table(Tl, list, count, kChunk);
@@ -476,7 +533,7 @@ mp_status run_pass(int pass, const mp_param* const* list, int n, const mp_adamw_
     first += count;
   } while (first < n);
   if (pass == 0 && clip.on) {
-    k_clip_finish<<<1, kFinishThreads, 0, s>>>(clip.tile_sums, tile_base, st, clip.max_norm);
+    k_clip_finish<<<kFoldCtas, 32, 0, s>>>(clip.tile_sums, tile_base, clip.warp_sums, st, clip.max_norm);
     note_launches(1);
     return launch_status();
   }
@@ -497,6 +554,10 @@ int64_t clip_tiles(const mp_param* params, int32_t n_params) {
   for (int i = 0; i < n_params; ++i)
     if (params[i].numel > 0) t += (params[i].numel + kTile - 1) / kTile;
   return t;
+}
+
+size_t clip_workspace_bytes(const mp_param* params, int32_t n_params) {
+  return kFoldBytes + (size_t)clip_tiles(params, n_params) * sizeof(float);
 }
 
 bool finite_f(float x) { return x == x && x - x == 0.0f; }
@@ -524,11 +585,12 @@ mp_status adamw_entry(int passes, const mp_param* params, int32_t n_params, mp_d
       !(hp->beta1 >= 0.0f && hp->beta1 < 1.0f) || !(hp->beta2 >= 0.0f && hp->beta2 < 1.0f) ||
       !finite_f(hp->max_grad_norm) || hp->max_grad_norm < 0.0f)
     return MP_EINVAL;
-  ClipArgs clip{(passes & 1) && hp->max_grad_norm > 0.0f, static_cast<float*>(d_workspace), hp->max_grad_norm};
+  unsigned char* ws = static_cast<unsigned char*>(d_workspace);
+  ClipArgs clip{(passes & 1) && hp->max_grad_norm > 0.0f, reinterpret_cast<double*>(ws),
+                reinterpret_cast<float*>(ws + kFoldBytes), hp->max_grad_norm};
   if (clip.on) {
-    if (!d_workspace || workspace_bytes < (size_t)clip_tiles(params, n_params) * sizeof(float))
-      return MP_EWORKSPACE;
-    if (reinterpret_cast<uintptr_t>(d_workspace) & 3u) return MP_EALIGN;
+    if (!d_workspace || workspace_bytes < clip_workspace_bytes(params, n_params)) return MP_EWORKSPACE;
+    if (reinterpret_cast<uintptr_t>(d_workspace) & 7u) return MP_EALIGN;
   }
   const mp_param* small[64];
   const mp_param** heap = nullptr;
@@ -563,8 +625,8 @@ mp_status adamw_entry(int passes, const mp_param* params, int32_t n_params, mp_d
 extern "C" {
 
 MP_API size_t mp_adamw_workspace_size(const mp_param* params, int32_t n_params) {
-  if (!params || n_params <= 0) return 0;
-  return (size_t)mp::clip_tiles(params, n_params) * sizeof(float);
+  if (n_params > 0 && !params) return 0;
+  return mp::clip_workspace_bytes(params, n_params < 0 ? 0 : n_params);
 }
 
 MP_API mp_status mp_adamw_step(const mp_param* params, int32_t n_params, mp_dtype grad_dtype,

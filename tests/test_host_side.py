@@ -54,6 +54,7 @@ def test_struct_layouts(M):
 
 def test_argument_validation_without_gpu(M):
     L = M.lib
+    launched0 = M.mp_launch_count()
     hp = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0)
     assert L.mp_adamw_step(None, 0, 9, M.MP_F16, ctypes.byref(hp), 16, None, 0, None) == M.MP_EINVAL
     assert L.mp_adamw_step(None, -1, M.MP_F16, M.MP_F16, ctypes.byref(hp), 16, None, 0, None) == M.MP_EINVAL
@@ -65,9 +66,12 @@ def test_argument_validation_without_gpu(M):
     # clipping needs a workspace of mp_adamw_workspace_size bytes
     clip = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, 1.0)
     p = (M.MpParam * 1)(M.MpParam(16, 16, 16, 16, 16, 40000))
-    assert L.mp_adamw_workspace_size(p, 1) == 4 * 3
+    need = 32 * 8 + 4 * 3  # binary64 warp partials + one binary32 sum per 16384-element tile
+    assert L.mp_adamw_workspace_size(p, 1) == need
+    assert L.mp_adamw_workspace_size(None, 0) == 32 * 8
     assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, None, 0, None) == M.MP_EWORKSPACE
-    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, 18, 12, None) == M.MP_EALIGN
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, 16, need - 1, None) == M.MP_EWORKSPACE
+    assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(clip), 16, 20, need, None) == M.MP_EALIGN
     neg = M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0, -1.0)
     assert L.mp_adamw_step(p, 1, M.MP_F16, M.MP_F16, ctypes.byref(neg), 16, None, 0, None) == M.MP_EINVAL
     cfg = M.ScalerCfg(2.0, 0.5, 0, 1)
@@ -99,7 +103,7 @@ def test_argument_validation_without_gpu(M):
     assert mx(16, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, 40, None) == M.MP_EALIGN
     assert mx(None, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, None, None) == M.MP_EINVAL
     assert mx(None, M.MP_BF16, 0, 64, M.MP_E2M1, None, None, None, None) == M.MP_OK
-    assert M.mp_launch_count() == 0
+    assert M.mp_launch_count() == launched0  # every rejected call returned before launching
 
 
 @pytest.mark.parametrize("b2,sr,rht", [(False, False, False), (False, True, True), (True, False, True), (True, True, False)])
