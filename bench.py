@@ -67,11 +67,18 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
-def dist_init(world):
+def dist_init(world, backend: str = "nccl"):
+    """One process per GPU over NCCL; the CPU tests use gloo."""
     if world > 1:
         import torch.distributed as dist
 
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
+
+
+def _backend():
+    import torch.distributed as dist
+
+    return dist.get_backend()
 
 
 def barrier(world):
@@ -79,7 +86,10 @@ def barrier(world):
         import torch
         import torch.distributed as dist
 
-        dist.barrier(device_ids=[torch.cuda.current_device()])
+        if _backend() == "nccl":
+            dist.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            dist.barrier()
 
 
 def max_over_ranks(x: float, world: int) -> float:
@@ -88,9 +98,17 @@ def max_over_ranks(x: float, world: int) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if _backend() == "nccl" else "cpu")
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_gbs(bytes_per_rank: float, elapsed_ms: float, world: int):
+    """Whole-job throughput: the bytes every rank processed over the slowest
+    rank's time (weak scaling: each rank runs the same work).  Returns
+    (GB/s, slowest rank's ms)."""
+    slowest = max_over_ranks(elapsed_ms, world)
+    return world * bytes_per_rank / (slowest * 1e-3) / 1e9, slowest
 
 
 # ---------------------------------------------------------------------------------------
@@ -271,6 +289,14 @@ class Workload:
         for q in self.q:
             self.bytes[q["name"]] = q["bytes"]
         self.step_bytes = sum(self.bytes.values())
+        # units (parameters or elements) per call, for elements/s
+        self.units = {"adamw_check": self.P, "adamw_apply": self.P, "loss_scale_update": 0,
+                      "fp8_act_e4m3": self.fp8_n, "fp8_grad_e5m2": self.fp8_n}
+        for q in self.q:
+            self.units[q["name"]] = q["rows"] * q["cols"]
+        self.units["fp8_act_e4m3_with_transpose"] = self.units["fp8_blockwise_1x128_act"] = self.fp8_n
+        self.units["fp8_blockwise_128x128_w"] = r.w_rows * r.w_cols
+        self.units["mxfp4_act"] = self.units["mxfp8_e4m3_act"] = r.act_rows * r.act_cols
 
     def step(self, k: int, ev=None):
         """Enqueue one step on the current stream; ev: list of len(calls)+1 events."""
@@ -503,6 +529,19 @@ class OracleSample:
             self.b[k] += by
         return t5 - t0
 
+    @staticmethod
+    def combined(samples):
+        """Per-part rates of concurrent samples add: returns an object whose
+        projected() uses the summed rates."""
+        class _Sum:
+            pass
+
+        out = _Sum()
+        out.t = {k: 1.0 for k in samples[0].t}
+        out.b = {k: sum(s.b[k] / s.t[k] for s in samples if s.t[k] > 0) for k in samples[0].t}
+        out.projected = lambda full: OracleSample.projected(out, full)
+        return out
+
     def sample_bytes(self):
         return sum(self.b.values())
 
@@ -539,6 +578,30 @@ WORKLOAD_NAME = ("llama3-8b fused adamw step (290 tensors, 8,030,257,152 params,
                  "[16384x5120] 1x16 rne + [5120x5120] 16x16 rne + [8192x12288] rht+1x16+sr")
 
 
+def cpu_all_cores(full_bytes, seconds: float = 8.0):
+    """The same oracle on every host core at once: one independent sample per
+    thread (the oracle's C calls release the GIL); per-part rates add up."""
+    import concurrent.futures as cf
+
+    n = os.cpu_count() or 1
+    samples = [OracleSample(scale=0.25) for _ in range(n)]
+    for s in samples:
+        s.run_once()
+        s.t = {k: 0.0 for k in s.t}
+        s.b = {k: 0.0 for k in s.b}
+    deadline = time.perf_counter() + seconds
+
+    def loop(s):
+        while time.perf_counter() < deadline:
+            s.run_once()
+
+    with cf.ThreadPoolExecutor(n) as ex:
+        list(ex.map(loop, samples))
+    total = OracleSample.combined(samples)
+    return {"value": round(total.projected(full_bytes), 4), "cores": n,
+            "sample": f"{n} threads, each: " + samples[0].describe().replace("oracle, 1 thread: ", "")}
+
+
 def cpu_baseline(full_bytes):
     s = OracleSample(scale=1.0)
     s.run_once()  # warm
@@ -547,8 +610,10 @@ def cpu_baseline(full_bytes):
     t0 = time.perf_counter()
     while time.perf_counter() - t0 < 12.0:
         s.run_once()
-    return {"value": round(s.projected(full_bytes), 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": s.describe()}
+    out = {"value": round(s.projected(full_bytes), 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": s.describe()}
+    out["all_cores"] = cpu_all_cores(full_bytes)
+    return out
 
 
 def run_reference(args):
@@ -616,7 +681,7 @@ def main():
     launches = M.mp_launch_count() - launches0
     barrier(world)
     clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_stop), world)
+    value, elapsed_ms = job_gbs(args.steps * wl.step_bytes, t_start.elapsed_time(t_stop), world)
 
     per_call_ms = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                    for i, name in enumerate(wl.calls)}
@@ -626,10 +691,10 @@ def main():
         ms = per_call_ms[name]
         gbs = wl.bytes[name] / (ms * 1e-3) / 1e9 if wl.bytes[name] else None
         kernels[name] = {"ms": round(ms, 4), "bytes": int(wl.bytes[name]),
+                         "elems_per_s": float(f"{wl.units[name] / (ms * 1e-3):.4g}") if wl.units[name] else None,
                          "gbs": round(gbs, 1) if gbs else None,
                          "frac_of_" + peak_kind + "_hbm": round(gbs / peak, 4) if gbs else None}
     ms_per_step = elapsed_ms / args.steps
-    value = world * wl.step_bytes / (ms_per_step * 1e-3) / 1e9
 
     apply_ms = per_call_ms["adamw_apply"]
     achieved = wl.bytes["adamw_apply"] / (apply_ms * 1e-3) / 1e9
@@ -649,6 +714,7 @@ def main():
             kernels[name] = {"bytes": int(wl.bytes[name]), "note": "not in the step; graph-replayed only"}
         gbs = wl.bytes[name] / (us * 1e-6) / 1e9
         kernels[name]["graph_isolated_us"] = round(us, 2)
+        kernels[name]["graph_isolated_elems_per_s"] = float(f"{wl.units[name] / (us * 1e-6):.4g}")
         kernels[name]["graph_isolated_gbs"] = round(gbs, 1)
         kernels[name]["graph_isolated_frac_of_" + peak_kind + "_hbm"] = round(gbs / peak, 4)
 
@@ -672,9 +738,8 @@ def main():
                 wl.e2e_step(k)
             b.record(stream)
             torch.cuda.synchronize()
-            e_ms = max_over_ranks(a.elapsed_time(b), world)
-            e2e = {"value": round(world * wl.step_bytes / (e_ms / args.steps * 1e-3) / 1e9, 1), "unit": UNIT,
-                   "ms_per_step": round(e_ms / args.steps, 3),
+            e_gbs, e_ms = job_gbs(args.steps * wl.step_bytes, a.elapsed_time(b), world)
+            e2e = {"value": round(e_gbs, 1), "unit": UNIT, "ms_per_step": round(e_ms / args.steps, 3),
                    "h2d_bytes_per_step": int(wl.h2d), "d2h_bytes_per_step": int(wl.d2h),
                    "api": "mp_adamw_step + loss_scale_update + fp8_cast_delayed x2 + nvfp4_quantize x3 "
                           "with pinned host inputs copied in and outputs copied out every step"}
