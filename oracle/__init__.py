@@ -16,7 +16,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 
-F32, F16, BF16, E4M3, E5M2, E2M1 = 0, 1, 2, 3, 4, 5
+F32, F16, BF16, E4M3, E5M2, E2M1, E2M3, E3M2 = 0, 1, 2, 3, 4, 5, 6, 7
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
 
@@ -149,7 +149,8 @@ def _p(a: np.ndarray | None):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-_NP = {F32: np.float32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8, E5M2: np.uint8, E2M1: np.uint8}
+_NP = {F32: np.float32, F16: np.uint16, BF16: np.uint16, E4M3: np.uint8, E5M2: np.uint8, E2M1: np.uint8,
+       E2M3: np.uint8, E3M2: np.uint8}
 
 
 def convert(x: np.ndarray, in_fmt: int, out_fmt: int) -> np.ndarray:

@@ -160,6 +160,31 @@ float orc_e2m1_to_f32(uint8_t c) {
   return sgn * (float)decode_mag(e, m, 1, 0, 1);
 }
 
+static void fp6_params(int fmt, int* M, int* emin, int* bias, double* maxv) {
+  if (fmt == ORC_E2M3) { *M = 3; *emin = 0; *bias = 1; *maxv = 7.5; }   /* 1.875 * 2^2 */
+  else { *M = 2; *emin = -2; *bias = 3; *maxv = 28.0; }                  /* 1.75 * 2^4 */
+}
+
+uint8_t orc_f32_to_fp6(float x, int fmt) {
+  int M, emin, bias;
+  double maxv;
+  fp6_params(fmt, &M, &emin, &bias, &maxv);
+  uint8_t s = signbit(x) ? 0x20 : 0;
+  double a = isinf(x) ? maxv : fabs((double)x);
+  double r = round_mag(a, M, emin);
+  if (r > maxv) r = maxv;
+  return s | (uint8_t)encode_mag(r, M, emin, bias);
+}
+
+float orc_fp6_to_f32(uint8_t c, int fmt) {
+  int M, emin, bias;
+  double maxv;
+  fp6_params(fmt, &M, &emin, &bias, &maxv);
+  uint32_t e = (c & 0x1F) >> M, m = c & ((1u << M) - 1);
+  float sgn = (c & 0x20) ? -1.0f : 1.0f;
+  return sgn * (float)decode_mag(e, m, M, emin, bias);
+}
+
 static float load_f32(const void* x, int fmt, int64_t i) {
   switch (fmt) {
     case ORC_F32: return ((const float*)x)[i];
@@ -167,6 +192,8 @@ static float load_f32(const void* x, int fmt, int64_t i) {
     case ORC_BF16: return orc_bf16_to_f32(((const uint16_t*)x)[i]);
     case ORC_E4M3: return orc_fp8_to_f32(((const uint8_t*)x)[i], ORC_E4M3);
     case ORC_E5M2: return orc_fp8_to_f32(((const uint8_t*)x)[i], ORC_E5M2);
+    case ORC_E2M3: return orc_fp6_to_f32(((const uint8_t*)x)[i], ORC_E2M3);
+    case ORC_E3M2: return orc_fp6_to_f32(((const uint8_t*)x)[i], ORC_E3M2);
     default: return orc_e2m1_to_f32(((const uint8_t*)x)[i]);
   }
 }
@@ -180,6 +207,8 @@ void orc_convert(const void* in, int in_fmt, int64_t n, void* out, int out_fmt) 
       case ORC_BF16: ((uint16_t*)out)[i] = orc_f32_to_bf16(v); break;
       case ORC_E4M3: ((uint8_t*)out)[i] = orc_f32_to_fp8_sat(v, ORC_E4M3); break;
       case ORC_E5M2: ((uint8_t*)out)[i] = orc_f32_to_fp8_sat(v, ORC_E5M2); break;
+      case ORC_E2M3: ((uint8_t*)out)[i] = orc_f32_to_fp6(v, ORC_E2M3); break;
+      case ORC_E3M2: ((uint8_t*)out)[i] = orc_f32_to_fp6(v, ORC_E3M2); break;
       default: ((uint8_t*)out)[i] = orc_f32_to_e2m1(v); break;
     }
   }
@@ -508,7 +537,7 @@ void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t 
 
 void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int elem_fmt, uint8_t* codes,
                      uint8_t* scales, uint16_t* dequant) {
-  int emax = elem_fmt == ORC_E4M3 ? 8 : (elem_fmt == ORC_E5M2 ? 15 : 2);
+  int emax = elem_fmt == ORC_E4M3 ? 8 : elem_fmt == ORC_E5M2 ? 15 : elem_fmt == ORC_E3M2 ? 4 : 2;
   int64_t nb = cols / 32;
   for (int64_t r = 0; r < rows; ++r) {
     for (int64_t b = 0; b < nb; ++b) {
@@ -536,7 +565,9 @@ void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int e
         uint8_t q = 0;
         if (!bad) {
           float y = load_f32(x, x_fmt, i) * mul;
-          q = (elem_fmt == ORC_E2M1) ? orc_f32_to_e2m1(y) : orc_f32_to_fp8_sat(y, elem_fmt);
+          q = elem_fmt == ORC_E2M1   ? orc_f32_to_e2m1(y)
+              : elem_fmt == ORC_E2M3 || elem_fmt == ORC_E3M2 ? orc_f32_to_fp6(y, elem_fmt)
+                                                              : orc_f32_to_fp8_sat(y, elem_fmt);
         }
         if (elem_fmt == ORC_E2M1) {
           uint8_t* byte = &codes[i >> 1];
@@ -546,8 +577,7 @@ void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int e
           codes[i] = q;
         }
         if (dequant) {
-          float v = bad ? 0.0f
-                        : (elem_fmt == ORC_E2M1 ? orc_e2m1_to_f32(q) : orc_fp8_to_f32(q, elem_fmt)) * (float)dq;
+          float v = bad ? 0.0f : load_f32(&q, elem_fmt, 0) * (float)dq;
           dequant[i] = orc_f32_to_bf16(v);
         }
       }

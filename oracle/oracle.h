@@ -33,7 +33,7 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E2M1 = 5 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_E4M3 = 3, ORC_E5M2 = 4, ORC_E2M1 = 5, ORC_E2M3 = 6, ORC_E3M2 = 7 };
 
 /* ---- number formats ---------------------------------------------------------
  * [MPT-ko] "왜 그냥 FP16으로는 안 되는가": FP16 = 5 exponent / 10 mantissa bits,
@@ -55,6 +55,13 @@ uint8_t orc_f32_to_e2m1(float x); /* finite x; |x| > 6 -> 6; sign kept on zero *
  * f16 = floor((|x| - lo) / (hi - lo) * 2^16); result hi iff f16 + r16 >= 2^16. */
 uint8_t orc_f32_to_e2m1_sr(float x, uint32_t r16);
 float orc_e2m1_to_f32(uint8_t c);
+/* FP6 ([MPT-ko] "FP8 혼합 정밀도" names MXFP6; layouts per reading R22):
+ * E2M3 = 1 sign, 2 exponent (bias 1), 3 mantissa bits, largest 7.5;
+ * E3M2 = 1 sign, 3 exponent (bias 3), 2 mantissa bits, largest 28.  No
+ * infinity or NaN.  A code is 6 bits: sign at bit 5.  RNE, saturating (the
+ * caller passes finite values). */
+uint8_t orc_f32_to_fp6(float x, int fmt);
+float orc_fp6_to_f32(uint8_t c, int fmt);
 /* Element-wise conversion between any two of the formats above. */
 void orc_convert(const void* in, int in_fmt, int64_t n, void* out, int out_fmt);
 /* amax = max |x| over n elements; any NaN gives the quiet NaN 0x7FC00000. */
@@ -176,7 +183,8 @@ void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t 
  * non-finite amax gives the scale byte 0xFF and all element codes 0.
  * codes: 1 byte per element (E4M3/E5M2) or two E2M1 codes per byte, element
  * 2j in the low nibble; scales [rows][cols / 32]; dequant (optional) is
- * BF16 RNE of value(code) * 2^e. */
+ * BF16 RNE of value(code) * 2^e.  MXFP6 (E2M3, emax 2; E3M2, emax 4) keeps
+ * one 6-bit code per byte (R22). */
 void orc_mx_quantize(const void* x, int x_fmt, int64_t rows, int64_t cols, int elem_fmt, uint8_t* codes,
                      uint8_t* scales, uint16_t* dequant);
 

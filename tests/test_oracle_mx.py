@@ -8,7 +8,20 @@ from tests.conftest import golden
 import oracle as O
 
 GRID = np.array(golden("nvfp4_format.json")["e2m1_magnitudes"])
-EMAX = {O.E4M3: 8, O.E5M2: 15, O.E2M1: 2}
+EMAX = {O.E4M3: 8, O.E5M2: 15, O.E2M1: 2, O.E2M3: 2, O.E3M2: 4}
+
+# FP6 magnitudes, codes 0..31 in order, written out from the bit layouts:
+# E2M3 subnormals k/8, then 1.000..1.875 x 2^0..2^2; E3M2 subnormals k/16,
+# then 1.00..1.75 x 2^-2..2^4.
+E2M3_MAGS = [0, .125, .25, .375, .5, .625, .75, .875,
+             1, 1.125, 1.25, 1.375, 1.5, 1.625, 1.75, 1.875,
+             2, 2.25, 2.5, 2.75, 3, 3.25, 3.5, 3.75,
+             4, 4.5, 5, 5.5, 6, 6.5, 7, 7.5]
+E3M2_MAGS = [0, .0625, .125, .1875, .25, .3125, .375, .4375,
+             .5, .625, .75, .875, 1, 1.25, 1.5, 1.75,
+             2, 2.5, 3, 3.5, 4, 5, 6, 7,
+             8, 10, 12, 14, 16, 20, 24, 28]
+FP6 = {O.E2M3: E2M3_MAGS, O.E3M2: E3M2_MAGS}
 
 
 def bf16(x):
@@ -20,7 +33,37 @@ def ue8m0_value(code):
     return torch.tensor(np.asarray(code, np.uint8)).view(torch.float8_e8m0fnu).float().numpy()
 
 
-@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2, O.E2M1])
+@pytest.mark.parametrize("fmt", [O.E2M3, O.E3M2])
+def test_fp6_decode_table(fmt):
+    codes = np.arange(64, dtype=np.uint8)
+    got = O.convert(codes, fmt, O.F32)
+    mags = np.array(FP6[fmt], np.float32)
+    np.testing.assert_array_equal(got[:32], mags)
+    np.testing.assert_array_equal(got[32:], -mags)
+
+
+@pytest.mark.parametrize("fmt", [O.E2M3, O.E3M2])
+def test_fp6_encode_brute_force_every_bf16(fmt):
+    """Nearest magnitude, ties to the even code, beyond the largest value
+    saturating, sign kept (also on zero): every finite BF16 pattern."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    x = O.convert(bits, O.BF16, O.F32)
+    fin = np.isfinite(x)
+    bits, x = bits[fin], x[fin]
+    got = O.convert(bits, O.BF16, fmt)
+    mags = np.array(FP6[fmt], np.float64)
+    a = np.minimum(np.abs(x.astype(np.float64)), mags[-1])
+    d = np.abs(a[:, None] - mags[None, :])
+    best = d.min(axis=1, keepdims=True)
+    cand = d == best
+    # among equidistant neighbours take the even code
+    idx = np.where(cand.sum(axis=1) > 1, np.argmax(cand & (np.arange(32)[None, :] % 2 == 0), axis=1),
+                   np.argmax(cand, axis=1))
+    want = idx.astype(np.uint8) | np.where(np.signbit(x), 0x20, 0).astype(np.uint8)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("fmt", [O.E4M3, O.E5M2, O.E2M1, O.E2M3, O.E3M2])
 def test_scale_exponent_closed_form(fmt):
     # each block's largest magnitude is a power of two 2^k (k from -20 to 20):
     # the scale is 2^(k - emax) and that element lands on 2^emax
