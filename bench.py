@@ -296,7 +296,7 @@ class Workload:
             self.units[q["name"]] = q["rows"] * q["cols"]
         self.units["fp8_act_e4m3_with_transpose"] = self.units["fp8_blockwise_1x128_act"] = self.fp8_n
         self.units["fp8_blockwise_128x128_w"] = r.w_rows * r.w_cols
-        self.units["mxfp4_act"] = self.units["mxfp8_e4m3_act"] = r.act_rows * r.act_cols
+        self.units["mxfp4_act"] = self.units["mxfp8_e4m3_act"] = self.units["mxfp6_e2m3_act"] = r.act_rows * r.act_cols
 
     def step(self, k: int, ev=None):
         """Enqueue one step on the current stream; ev: list of len(calls)+1 events."""
@@ -388,6 +388,8 @@ class Workload:
         self.extra_bytes["mxfp4_act"] = (2.5 + 1.0 / 32) * n_a
         calls["mxfp8_e4m3_act"] = lambda k: M.mx_quantize(pick(ar, k), pick(mx_c, k), pick(mx_s, k), M.MP_E4M3)
         self.extra_bytes["mxfp8_e4m3_act"] = (3.0 + 1.0 / 32) * n_a
+        calls["mxfp6_e2m3_act"] = lambda k: M.mx_quantize(pick(ar, k), pick(mx_c, k), pick(mx_s, k), M.MP_E2M3)
+        self.extra_bytes["mxfp6_e2m3_act"] = (3.0 + 1.0 / 32) * n_a  # one FP6 code per byte
         for q in self.q:
             qc, qs = rot(q["codes"], clone=False), rot(q["scales"], clone=False)
             calls[q["name"]] = (lambda q, xr, qc, qs: lambda k: M.nvfp4_quantize(

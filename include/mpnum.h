@@ -59,7 +59,7 @@ enum {
 };
 
 typedef int32_t mp_dtype;
-enum { MP_F32 = 0, MP_F16 = 1, MP_BF16 = 2, MP_E4M3 = 3, MP_E5M2 = 4, MP_E2M1 = 5 };
+enum { MP_F32 = 0, MP_F16 = 1, MP_BF16 = 2, MP_E4M3 = 3, MP_E5M2 = 4, MP_E2M1 = 5, MP_E2M3 = 6, MP_E3M2 = 7 };
 
 MP_API const char* mp_status_str(mp_status s);
 MP_API int32_t mp_version(void);
@@ -329,15 +329,18 @@ MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t 
  * power-of-two scale for every 32 elements, MXFP8 and MXFP4; [NVFP4] §2.1:
  * MXFP4 keeps a UE8M0 scale byte per 32-element block).  x [rows, cols]
  * (x_dtype MP_F32, MP_F16 or MP_BF16, row-major); every run of 32 elements
- * along a row is a block.  elem_dtype MP_E4M3, MP_E5M2 (MXFP8) or MP_E2M1
+ * along a row is a block.  elem_dtype MP_E4M3, MP_E5M2 (MXFP8), MP_E2M3,
+ * MP_E3M2 (MXFP6: 1 sign, 2 exponent (bias 1), 3 mantissa bits, largest 7.5;
+ * 1 sign, 3 exponent (bias 3), 2 mantissa bits, largest 28) or MP_E2M1
  * (MXFP4).  For a block with amax = max |x| finite: e = floor(log2 amax) -
- * emax (emax 8, 15, 2: the exponent of the element format's largest value),
+ * emax (emax 8, 15, 2, 4, 2: the exponent of the element format's largest value),
  * clamped below at -127 (so amax = 0 or subnormal gives -127); scales[block]
  * = e + 127 (UE8M0, [rows][cols/32], one byte per block); each element is
  * saturate(RNE(fp32(x) * 2^-e)) in elem_dtype.  A block holding an infinity
  * or NaN gets the scale byte 0xFF (the UE8M0 NaN) and all-zero codes.
- * codes: one byte per element for FP8, or two E2M1 codes per byte (element
- * 2j in the low nibble), row-major.  dequant_bf16 (may be NULL): BF16 RNE of
+ * codes: one byte per element for FP8 and FP6 (an FP6 code in bits 0..5, sign
+ * at bit 5, bits 6..7 zero), or two E2M1 codes per byte (element 2j in the
+ * low nibble), row-major.  dequant_bf16 (may be NULL): BF16 RNE of
  * value(code) * 2^e, zero for a non-finite block.  cols % 32 == 0 (else
  * MP_ESHAPE); x, codes and dequant_bf16 16-byte aligned.  One kernel launch;
  * rows * cols == 0 launches nothing. */

@@ -19,7 +19,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmpnum.so")
 
 MP_OK, MP_EINVAL, MP_EALIGN, MP_ESHAPE, MP_EWORKSPACE, MP_ECUDA = 0, -1, -2, -3, -4, -5
-MP_F32, MP_F16, MP_BF16, MP_E4M3, MP_E5M2, MP_E2M1 = 0, 1, 2, 3, 4, 5
+MP_F32, MP_F16, MP_BF16, MP_E4M3, MP_E5M2, MP_E2M1, MP_E2M3, MP_E3M2 = 0, 1, 2, 3, 4, 5, 6, 7
 
 
 class MpParam(ctypes.Structure):
@@ -345,7 +345,7 @@ def rht16(x, y, sign_mask: int, stream=None) -> None:
 
 
 def mx_quantize(x, codes, scales, elem_dtype: int = MP_E2M1, dequant=None, stream=None) -> None:
-    """x: [rows, cols], cols % 32 == 0; codes: rows*cols bytes (FP8) or
+    """x: [rows, cols], cols % 32 == 0; codes: rows*cols bytes (FP8, FP6) or
     rows*cols/2 (E2M1); scales: uint8 [rows, cols/32] (UE8M0)."""
     rows, cols = x.shape
     _check("mx_quantize", lib.mx_quantize(_ptr(x), _dtype_code(x), rows, cols, elem_dtype, _ptr(codes),
@@ -354,7 +354,7 @@ def mx_quantize(x, codes, scales, elem_dtype: int = MP_E2M1, dequant=None, strea
 
 __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
-    "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2", "MP_E2M1", "mx_quantize",
+    "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2", "MP_E2M1", "MP_E2M3", "MP_E3M2", "mx_quantize",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
     "fp8_cast_transpose_delayed", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",

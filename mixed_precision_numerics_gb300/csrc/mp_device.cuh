@@ -70,6 +70,18 @@ __device__ __forceinline__ uint32_t cvt_e2m1x2(float lo, float hi) {
   asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u16.u8 %0, t; }" : "=h"(r) : "f"(hi), "f"(lo));
   return r;
 }
+// Packed FP6 pair (one 6-bit code per byte, upper two bits zero), round to
+// nearest even, saturating at the largest finite value: lo -> bits 0..7.
+__device__ __forceinline__ uint32_t cvt_e2m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_e3m2x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e3m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
 // Non-negative finite E4M3 byte (0x00..0x7E) -> float, exact.  Normal codes
 // rebias the exponent field (7 -> 127); subnormals are m * 2^-9.
 __device__ __forceinline__ float e4m3_pos_to_f32(uint32_t code) {

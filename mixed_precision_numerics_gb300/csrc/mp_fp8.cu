@@ -202,46 +202,79 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
 }
 
 // Cast of a [rows, cols] tensor that also writes the transposed bytes
-// y_t [cols, rows] from the same read: a CTA takes a 64 x 64 tile, casts it
-// (each thread one 16-element row segment), stores the rows of y, stages the
-// bytes in shared memory and stores 16-byte column segments of y_t.
-constexpr int kTT = 64;  // tile edge
+// y_t [cols, rows] from the same read.  A CTA takes a 128 x 128 tile: thread
+// t casts the 16-element row segments (t % 8) of rows t / 8 + 32 k, k = 0..3
+// (128 B of input in flight), stores them to y and to a row-major copy of the
+// tile in shared memory.  After one barrier, thread t reads the 32-bit words
+// of column group t % 32 (columns 4 (t % 32) .. + 3) for rows 16 (t / 32) ..
+// + 15 -- each read instruction takes one row's 32 consecutive words, free of
+// bank conflicts -- transposes the 4 x 4 byte blocks with byte permutes and
+// stores four 16-byte row segments of y_t.
+constexpr int kTT = 128;  // tile edge
+
+// 4 x 4 byte transpose: w[i] holds row i (byte j = column j); returns in
+// c[j] the column j (byte i = row i).
+__device__ __forceinline__ void transpose4x4(const uint32_t (&w)[4], uint32_t (&c)[4]) {
+  const uint32_t a0 = __byte_perm(w[0], w[1], 0x5140), a1 = __byte_perm(w[0], w[1], 0x7362);
+  const uint32_t a2 = __byte_perm(w[2], w[3], 0x5140), a3 = __byte_perm(w[2], w[3], 0x7362);
+  c[0] = __byte_perm(a0, a2, 0x5410);
+  c[1] = __byte_perm(a0, a2, 0x7632);
+  c[2] = __byte_perm(a1, a3, 0x5410);
+  c[3] = __byte_perm(a1, a3, 0x7632);
+}
+
 template <int XT, bool E5M2>
 __global__ __launch_bounds__(kThreads) void k_fp8_cast_t(const void* __restrict__ x, int64_t rows, int64_t cols,
                                                          uint8_t* __restrict__ y, uint8_t* __restrict__ y_t,
                                                          mp_fp8_meta* meta, float* hist, int32_t hist_len,
                                                          float margin, int32_t algo) {
+  constexpr int kRowsPerPass = kThreads / 8;  // 32 rows of 8 segments per pass over the tile
   __shared__ uint32_t red[32];
   __shared__ int is_last;
-  __shared__ __align__(16) uint8_t tile[kTT][kTT + 16];  // 80-byte pitch: 16-byte row segments stay aligned
+  __shared__ __align__(16) uint8_t tile[kTT][kTT];
   const float scale = meta->scale;
   const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;
   if (blockIdx.x == 0 && algo == 0) fold_history_rest(meta, hist, hist_len, slot, red);
   const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
-  const int lr = threadIdx.x >> 2, seg = (threadIdx.x & 3) * 16;  // row in tile, column segment
+  const int lr = threadIdx.x >> 3, seg = (threadIdx.x & 7) * 16;  // row (pass 0) and column segment
+  const int cw = threadIdx.x & 31, rs = (threadIdx.x >> 5) * 16;   // transposed: column group, row run
   float acc = 0.0f;
   for (int64_t tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
     const int64_t r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
-    const int64_t row = r0 + lr, col = c0 + seg;
-    if (row < rows && col < cols) {
-      uint4 raw[4];
-      load_raw<XT>(x, (row * cols + col) / kElems, raw);
-      float vmax;
-      const uint4 o = cast16<XT, E5M2>(raw, scale, &vmax);
-      acc = max_abs_nan(acc, vmax);
-      st_cs(y + row * cols + col, o);
-      *reinterpret_cast<uint4*>(&tile[lr][seg]) = o;
+    const int64_t col = c0 + seg;
+    uint4 raw[kTT / kRowsPerPass][4];
+#pragma unroll
+    for (int k = 0; k < kTT / kRowsPerPass; ++k) {
+      const int64_t row = r0 + lr + kRowsPerPass * k;
+      if (row < rows && col < cols) load_raw<XT>(x, (row * cols + col) / kElems, raw[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < kTT / kRowsPerPass; ++k) {
+      const int64_t row = r0 + lr + kRowsPerPass * k;
+      if (row < rows && col < cols) {
+        float vmax;
+        const uint4 o = cast16<XT, E5M2>(raw[k], scale, &vmax);
+        acc = max_abs_nan(acc, vmax);
+        st_cs(y + row * cols + col, o);
+        *reinterpret_cast<uint4*>(&tile[lr + kRowsPerPass * k][seg]) = o;
+      }
     }
     __syncthreads();
-    // transposed: thread handles column lr of the tile, rows seg .. seg + 15
-    const int64_t tcol = c0 + lr, trow = r0 + seg;
-    if (tcol < cols && trow < rows) {
-      uint32_t w[4];
+    const int64_t tcol = c0 + 4 * cw, trow = r0 + rs;
+    if (tcol < cols && trow < rows) {  // cols and rows are multiples of 16: the 4 columns and 16 rows are all in
+      uint32_t out[4][4];  // out[j][m]: column j, rows rs + 4m .. + 3
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        w[q] = (uint32_t)tile[seg + 4 * q][lr] | ((uint32_t)tile[seg + 4 * q + 1][lr] << 8) |
-               ((uint32_t)tile[seg + 4 * q + 2][lr] << 16) | ((uint32_t)tile[seg + 4 * q + 3][lr] << 24);
-      st_cs(y_t + tcol * rows + trow, make_uint4(w[0], w[1], w[2], w[3]));
+      for (int m = 0; m < 4; ++m) {
+        uint32_t w[4], c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[rs + 4 * m + i][4 * cw]);
+        transpose4x4(w, c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[j][m] = c[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_cs(y_t + (tcol + j) * rows + trow, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
     }
     __syncthreads();  // the tile is rewritten by the next iteration
   }
@@ -261,45 +294,63 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
   *r = (isfinite(amax) && amax > 0.0f) ? __fdiv_rn(fmax, amax) : 0.0f;
 }
 
+// Quads per warp iteration.  Deeper unrolls (2 or 4 quads, 64-128 B in flight
+// per thread) measured slower on the [8192 x 4096] activations: their register
+// use cuts the resident CTAs per SM more than the extra loads in flight help.
+template <int XT>
+__host__ __device__ constexpr int quads_of() { return 1; }
+
 // 1 x 128 tiles: eight threads per tile (16 elements each), four tiles per
-// warp; the loop runs over warp-sized groups of tiles so that every lane
-// takes part in the width-8 shuffles.
+// warp ("a quad"); each warp takes U quads per iteration with all their loads
+// issued first.  Quad validity is uniform across the warp, so every lane takes
+// part in the width-8 shuffles.
 template <int XT, bool E5M2>
 __global__ __launch_bounds__(kThreads) void k_fp8_block_1x128(const void* __restrict__ x, int64_t rows,
                                                               int64_t cols, uint8_t* __restrict__ y,
                                                               float* __restrict__ scales) {
+  constexpr int U = quads_of<XT>();
+  constexpr int kWarps = kThreads / 32;
   const int64_t ntc = (cols + 127) / 128;
   const int64_t ntiles = rows * ntc;
   const int64_t nquads = (ntiles + 3) / 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 3, l8 = lane & 7;
-  const int64_t wstride = (int64_t)gridDim.x * (kThreads / 32);
-  for (int64_t q = (int64_t)blockIdx.x * (kThreads / 32) + warp; q < nquads; q += wstride) {
-    const int64_t tile = q * 4 + g;
-    const int64_t row = tile / ntc, tc = tile % ntc;
-    const int64_t col = tc * 128 + l8 * 16;
-    const bool valid = tile < ntiles && col < cols;
-    uint4 raw[4];
-    float vmax = 0.0f;
-    if (valid) {
-      load_raw<XT>(x, (row * cols + col) / kElems, raw);
+  for (int64_t q0 = (int64_t)blockIdx.x * kWarps * U + warp; q0 < nquads; q0 += (int64_t)gridDim.x * kWarps * U) {
+    uint4 raw[U][4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const float2 f = pair_of<XT>(raw, k);
-        vmax = max_abs_nan(vmax, f.x);
-        vmax = max_abs_nan(vmax, f.y);
+    for (int u = 0; u < U; ++u) {
+      const int64_t tile = (q0 + (int64_t)u * kWarps) * 4 + g;
+      const int64_t row = tile / ntc, col = (tile % ntc) * 128 + l8 * 16;
+      if (tile < ntiles && col < cols) load_raw<XT>(x, (row * cols + col) / kElems, raw[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t q = q0 + (int64_t)u * kWarps;
+      if (q >= nquads) break;  // warp-uniform
+      const int64_t tile = q * 4 + g;
+      const int64_t row = tile / ntc, tc = tile % ntc;
+      const int64_t col = tc * 128 + l8 * 16;
+      const bool valid = tile < ntiles && col < cols;
+      float vmax = 0.0f;
+      if (valid) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 f = pair_of<XT>(raw[u], k);
+          vmax = max_abs_nan(vmax, f.x);
+          vmax = max_abs_nan(vmax, f.y);
+        }
       }
-    }
 #pragma unroll
-    for (int h = 4; h >= 1; h >>= 1) {
-      const float o = __shfl_xor_sync(0xFFFFFFFFu, vmax, h, 8);
-      vmax = max_abs_nan(vmax, o);
+      for (int h = 4; h >= 1; h >>= 1) {
+        const float o = __shfl_xor_sync(0xFFFFFFFFu, vmax, h, 8);
+        vmax = max_abs_nan(vmax, o);
+      }
+      if (!valid) continue;
+      const float amax = vmax != vmax ? __uint_as_float(0x7FC00000u) : vmax;
+      float s, r, unused;
+      block_scale_of<E5M2>(amax, &s, &r);
+      st_cs(y + row * cols + col, cast16<XT, E5M2>(raw[u], r, &unused));
+      if (l8 == 0) scales[row * ntc + tc] = s;
     }
-    if (!valid) continue;
-    const float amax = vmax != vmax ? __uint_as_float(0x7FC00000u) : vmax;
-    float s, r, unused;
-    block_scale_of<E5M2>(amax, &s, &r);
-    st_cs(y + row * cols + col, cast16<XT, E5M2>(raw, r, &unused));
-    if (l8 == 0) scales[row * ntc + tc] = s;
   }
 }
 
@@ -387,7 +438,8 @@ mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool squar
   } else {
     static const int occ = occ_of(k_fp8_block_1x128<XT, E5M2>);
     const int64_t quads = (rows * ((cols + 127) / 128) + 3) / 4;
-    const int64_t ctas = (quads + kThreads / 32 - 1) / (kThreads / 32);
+    const int64_t per_cta = (int64_t)(kThreads / 32) * quads_of<XT>();
+    const int64_t ctas = (quads + per_cta - 1) / per_cta;
     k_fp8_block_1x128<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, rows, cols, y, scales);
   }
   note_launches(1);

@@ -1,7 +1,8 @@
 // mp_mx.cu — MX block formats: one power-of-two scale per 32 elements.
 //
 // [MPT-ko] itwiki "혼합 정밀도 학습", "FP8 혼합 정밀도" (microscaling: a
-// power-of-two scale for every 32 elements, MXFP8 / MXFP6 / MXFP4); [NVFP4]
+// power-of-two scale for every 32 elements, MXFP8 / MXFP6 / MXFP4; FP6 codes
+// are kept one per byte, as the hardware conversion produces them); [NVFP4]
 // gist.science "Pretraining Large Language Models with NVFP4", §2.1 (MXFP4:
 // 32-element blocks, UE8M0 scale byte).  The scale exponent follows the OCP
 // microscaling rule, e = floor(log2 amax) - emax_elem, so the block maximum
@@ -23,14 +24,16 @@ constexpr int kThreads = 256;
 constexpr int kBlock = 32;
 
 enum { XF32 = 0, XF16 = 1, XBF16 = 2 };
-enum { EE4M3 = 0, EE5M2 = 1, EE2M1 = 2 };
+enum { EE4M3 = 0, EE5M2 = 1, EE2M1 = 2, EE2M3 = 3, EE3M2 = 4 };
 
 template <int XT>
 __host__ __device__ constexpr int words_of() { return XT == XF32 ? 8 : 4; }  // uint4 per block
 template <int XT>
 __host__ __device__ constexpr int unroll_of() { return XT == XF32 ? 1 : 2; }
 template <int EF>
-__host__ __device__ constexpr uint32_t emax_of() { return EF == EE4M3 ? 8u : (EF == EE5M2 ? 15u : 2u); }
+__host__ __device__ constexpr uint32_t emax_of() {
+  return EF == EE4M3 ? 8u : EF == EE5M2 ? 15u : EF == EE3M2 ? 4u : 2u;  // E2M1 and E2M3: 2
+}
 
 // Element pair k (elements 2k, 2k+1) of a block held as raw 16-byte words.
 template <int XT>
@@ -47,10 +50,20 @@ __device__ __forceinline__ float2 pair_at(const uint4* r, int k) {
 }
 
 // Exact value of an element code.  E5M2 is the upper byte of a binary16;
-// E4M3 rebiases (sign applied separately); E2M1 reads its magnitude table.
+// E4M3 rebiases (sign applied separately); E2M1 reads its magnitude table;
+// FP6 (sign at bit 5) is mantissa-with-hidden-bit times a power of two.
 template <int EF>
 __device__ __forceinline__ float code_value(uint32_t c) {
-  if constexpr (EF == EE5M2) {
+  if constexpr (EF == EE2M3 || EF == EE3M2) {
+    constexpr uint32_t kM = EF == EE2M3 ? 3u : 2u;           // mantissa bits
+    constexpr int kBias = EF == EE2M3 ? 1 : 3;
+    const uint32_t e = (c & 0x1Fu) >> kM, m = c & ((1u << kM) - 1u);
+    // subnormal: m * 2^(1 - bias - M); normal: (2^M + m) * 2^(e - bias - M)
+    const float sig = (float)(e ? (m | (1u << kM)) : m);
+    const int ex = (e ? (int)e : 1) - kBias - (int)kM;
+    const float v = __fmul_rn(sig, __uint_as_float((uint32_t)(127 + ex) << 23));
+    return (c & 0x20u) ? -v : v;
+  } else if constexpr (EF == EE5M2) {
     return __half2float(__ushort_as_half((unsigned short)(c << 8)));
   } else if constexpr (EF == EE4M3) {
     const float v = e4m3_pos_to_f32(c & 0x7Fu);
@@ -60,13 +73,17 @@ __device__ __forceinline__ float code_value(uint32_t c) {
   }
 }
 
-// Saturating RNE code pair of two scaled finite values; FP8 pairs occupy 16
-// bits (element 2k in the low byte), E2M1 pairs 8 bits (element 2k in the low
-// nibble).
+// Saturating RNE code pair of two scaled finite values; FP8 and FP6 pairs
+// occupy 16 bits (element 2k in the low byte), E2M1 pairs 8 bits (element 2k
+// in the low nibble).
 template <int EF>
 __device__ __forceinline__ uint32_t encode_pair(float a, float b) {
   if constexpr (EF == EE2M1) {
     return cvt_e2m1x2(a, b);
+  } else if constexpr (EF == EE2M3) {
+    return cvt_e2m3x2(a, b);
+  } else if constexpr (EF == EE3M2) {
+    return cvt_e3m2x2(a, b);
   } else {
     constexpr float fmax = EF == EE5M2 ? 57344.0f : 448.0f;
     a = fminf(fmaxf(a, -fmax), fmax);
@@ -94,7 +111,7 @@ __device__ __forceinline__ void mx_block(const uint4* raw, int64_t blk, uint8_t*
   constexpr uint32_t emax = emax_of<EF>();
   const uint32_t sb = bad ? 0xFFu : (E > emax ? E - emax : 0u);
   const float mul = __uint_as_float((254u - (bad ? 0u : sb)) << 23);  // 2^-e, a normal binary32
-  uint32_t w[8];  // FP8: 8 words of 4 codes; E2M1: 4 words of 8 codes
+  uint32_t w[8];  // FP8 / FP6: 8 words of 4 one-byte codes; E2M1: 4 words of 8 codes
 #pragma unroll
   for (int k = 0; k < kBlock / 2; ++k) {
     const float2 f = pair_at<XT>(raw, k);
@@ -188,6 +205,8 @@ mp_status launch_x(int32_t elem, const void* x, int64_t nblk, uint8_t* codes, ui
   switch (elem) {
     case MP_E4M3: return launch<XT, EE4M3>(x, nblk, codes, scales, dq, s);
     case MP_E5M2: return launch<XT, EE5M2>(x, nblk, codes, scales, dq, s);
+    case MP_E2M3: return launch<XT, EE2M3>(x, nblk, codes, scales, dq, s);
+    case MP_E3M2: return launch<XT, EE3M2>(x, nblk, codes, scales, dq, s);
     default: return launch<XT, EE2M1>(x, nblk, codes, scales, dq, s);
   }
 }
@@ -201,7 +220,9 @@ extern "C" MP_API mp_status mx_quantize(const void* x, mp_dtype x_dtype, int64_t
   using namespace mp;
   if (rows < 0 || cols < 0) return MP_EINVAL;
   if (x_dtype != MP_F32 && x_dtype != MP_F16 && x_dtype != MP_BF16) return MP_EINVAL;
-  if (elem_dtype != MP_E4M3 && elem_dtype != MP_E5M2 && elem_dtype != MP_E2M1) return MP_EINVAL;
+  if (elem_dtype != MP_E4M3 && elem_dtype != MP_E5M2 && elem_dtype != MP_E2M1 && elem_dtype != MP_E2M3 &&
+      elem_dtype != MP_E3M2)
+    return MP_EINVAL;
   const int64_t n = rows * cols;
   if (n > 0 && (!x || !codes || !scales)) return MP_EINVAL;
   if (cols % kBlock != 0) return MP_ESHAPE;

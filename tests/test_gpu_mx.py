@@ -14,7 +14,7 @@ import mixed_precision_numerics_gb300 as M  # noqa: E402
 
 pytestmark = pytest.mark.gpu
 XFMT = {torch.float32: O.F32, torch.float16: O.F16, torch.bfloat16: O.BF16}
-EFMT = {M.MP_E4M3: O.E4M3, M.MP_E5M2: O.E5M2, M.MP_E2M1: O.E2M1}
+EFMT = {M.MP_E4M3: O.E4M3, M.MP_E5M2: O.E5M2, M.MP_E2M1: O.E2M1, M.MP_E2M3: O.E2M3, M.MP_E3M2: O.E3M2}
 
 
 @pytest.fixture(autouse=True)
@@ -58,7 +58,7 @@ def check(x, xfmt, xt, elem):
     np.testing.assert_array_equal(d, rd)
 
 
-@pytest.mark.parametrize("elem", [M.MP_E4M3, M.MP_E5M2, M.MP_E2M1])
+@pytest.mark.parametrize("elem", [M.MP_E4M3, M.MP_E5M2, M.MP_E2M1, M.MP_E2M3, M.MP_E3M2])
 @pytest.mark.parametrize("shape", [(1, 32), (3, 96), (7, 544), (129, 1056), (257, 4096)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 def test_small_shapes(elem, shape, dtype):
@@ -74,7 +74,7 @@ def test_without_dequant():
     np.testing.assert_array_equal(c, rc)
 
 
-@pytest.mark.parametrize("elem", [M.MP_E2M1, M.MP_E4M3])
+@pytest.mark.parametrize("elem", [M.MP_E2M1, M.MP_E4M3, M.MP_E2M3, M.MP_E3M2])
 def test_full_size_activation(elem):
     c = W.NVFP4_RNE
     x = torch.empty((c.act_rows, c.act_cols), dtype=torch.bfloat16, device="cuda")
@@ -94,6 +94,24 @@ def test_full_size_gradient_e5m2():
     rc, rs, _ = O.mx_quantize(to_host(x, np.uint16).reshape(c.rows, c.cols), O.BF16, O.E5M2, want_dequant=False)
     assert np.array_equal(gs, rs)
     assert np.array_equal(gc, rc)
+
+
+def test_fp6_every_bf16_magnitude_on_a_unit_scale():
+    """Blocks whose maximum is 2^emax (scale 2^0) carry every BF16 value in
+    [-2^(emax+1), 2^(emax+1)): the FP6 codes are the format's own rounding."""
+    for elem, emax in ((M.MP_E2M3, 2), (M.MP_E3M2, 4)):
+        bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+        v = O.convert(bits, O.BF16, O.F32)
+        v = v[np.isfinite(v) & (np.abs(v) < 2.0 ** (emax + 1))]
+        n = -(-v.size // 31) * 31
+        v = np.concatenate([v, np.zeros(n - v.size, np.float32)]).reshape(-1, 31)
+        x = np.concatenate([np.full((v.shape[0], 1), 2.0 ** emax, np.float32), v], axis=1)
+        xb = O.convert(x, O.F32, O.BF16)
+        c, s, d = gpu_mx(to_dev(xb, torch.bfloat16), elem)
+        rc, rs, rd = O.mx_quantize(xb, O.BF16, EFMT[elem])
+        assert (rs == 127).all()
+        np.testing.assert_array_equal(c, rc)
+        np.testing.assert_array_equal(d, rd)
 
 
 def test_errors():

@@ -99,6 +99,8 @@ def test_argument_validation_without_gpu(M):
     assert mx(16, M.MP_BF16, 2, 48, M.MP_E4M3, 16, 16, None, None) == M.MP_ESHAPE
     assert mx(16, M.MP_BF16, 2, 64, M.MP_F16, 16, 16, None, None) == M.MP_EINVAL
     assert mx(16, M.MP_E4M3, 2, 64, M.MP_E2M1, 16, 16, None, None) == M.MP_EINVAL
+    assert mx(16, M.MP_BF16, 2, 64, 8, 16, 16, None, None) == M.MP_EINVAL
+    assert mx(16, M.MP_BF16, 2, 48, M.MP_E3M2, 16, 16, None, None) == M.MP_ESHAPE
     assert mx(16, M.MP_BF16, 2, 64, M.MP_E2M1, 8, 16, None, None) == M.MP_EALIGN
     assert mx(16, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, 40, None) == M.MP_EALIGN
     assert mx(None, M.MP_BF16, 2, 64, M.MP_E2M1, 16, 16, None, None) == M.MP_EINVAL
