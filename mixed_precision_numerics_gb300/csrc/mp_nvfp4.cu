@@ -15,6 +15,9 @@
 //   k_nvfp4_1x16 /  read x again, recompute x', form block scales, encode,
 //   k_nvfp4_2d      pack two codes per byte (0.5 B/elem) and one scale byte
 //                   per block.
+// For 1x16 the amax pass loads the last half-L2's worth of x with the L2
+// evict-last policy and the encode pass walks x from the end, so that part
+// of the second read is served by L2.
 // The transform is evaluated on CUDA cores by the butterfly in binary32 so
 // that its additions happen in the documented order.
 #include <mutex>
@@ -33,10 +36,9 @@ struct Ws {
   uint32_t ticket;
 };
 
-// Load one 16-element tile of BF16 and produce x' in binary32.
+// x' in binary32 of one 16-element BF16 tile given as two 16-byte words.
 template <bool RHT>
-__device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw, float (&v)[16]) {
-  uint4 a = ld_plain(p), b = ld_plain(p + 8);
+__device__ __forceinline__ void tile_values(uint4 a, uint4 b, const SignWords& sw, float (&v)[16]) {
   if (RHT) apply_signs(a, b, sw);
   unpack_bf16x16(a, b, v);
   if (RHT) {
@@ -46,15 +48,22 @@ __device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw
   }
 }
 
+// Load one 16-element tile of BF16 and produce x' in binary32.
+template <bool RHT>
+__device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw, float (&v)[16]) {
+  tile_values<RHT>(ld_plain(p), ld_plain(p + 8), sw, v);
+}
+
 template <bool RHT>
 __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restrict__ x, int64_t ntiles,
                                                          uint32_t mask, Ws* ws, float* tensor_scale,
-                                                         int32_t* nonfinite) {
+                                                         int32_t* nonfinite, int64_t keep_from) {
   __shared__ uint32_t red[32];
   __shared__ int is_last;
   const SignWords sw = sign_words(mask);
   float acc = 0.0f;
   constexpr int U = 2;
+  const uint64_t keep = policy_evict_last();
   const int64_t step = (int64_t)gridDim.x * kThreads * U;
   for (int64_t t0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; t0 < ntiles; t0 += step) {
     uint4 a[U], b[U];
@@ -62,8 +71,13 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restr
     for (int u = 0; u < U; ++u) {
       const int64_t t = t0 + (int64_t)u * kThreads;
       if (t < ntiles) {
-        a[u] = ld_plain(x + t * 16);
-        b[u] = ld_plain(x + t * 16 + 8);
+        if (t >= keep_from) {
+          a[u] = ld_hint(x + t * 16, keep);
+          b[u] = ld_hint(x + t * 16 + 8, keep);
+        } else {
+          a[u] = ld_plain(x + t * 16);
+          b[u] = ld_plain(x + t * 16 + 8);
+        }
       }
     }
 #pragma unroll
@@ -191,7 +205,10 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
   const SignWords sw = sign_words(mask);
   const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
-  for (int64_t blk = (int64_t)blockIdx.x * kThreads + threadIdx.x; blk < nblocks; blk += stride) {
+  const uint64_t last_use = policy_evict_first();  // this pass is the last reader of x
+  for (int64_t i = (int64_t)blockIdx.x * kThreads + threadIdx.x; i < nblocks; i += stride) {
+    // Last block first: the amax pass marked the tail of x to stay in L2.
+    const int64_t blk = nblocks - 1 - i;
     if (zero) {
       *reinterpret_cast<uint2*>(codes + blk * 8) = make_uint2(0u, 0u);
       scales[blk] = 0;
@@ -202,7 +219,7 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
       continue;
     }
     float v[16];
-    load_tile<RHT>(x + blk * 16, sw, v);
+    tile_values<RHT>(ld_hint(x + blk * 16, last_use), ld_hint(x + blk * 16 + 8, last_use), sw, v);
     float bamax = 0.0f;
 #pragma unroll
     for (int j = 0; j < 16; ++j) bamax = fmaxf(bamax, fabsf(v[j]));
@@ -303,10 +320,28 @@ int occ_of(K kernel) {
 }
 
 template <bool RHT>
-void launch_amax(const uint16_t* x, int64_t ntiles, uint32_t mask, Ws* ws, float* ts, int32_t* nf, cudaStream_t s) {
+void launch_amax(const uint16_t* x, int64_t ntiles, uint32_t mask, Ws* ws, float* ts, int32_t* nf, int64_t keep_from,
+                 cudaStream_t s) {
   static const int occ = occ_of(k_nvfp4_amax<RHT>);
   const int64_t ctas = (ntiles + 2 * kThreads - 1) / (2 * kThreads);
-  k_nvfp4_amax<RHT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, mask, ws, ts, nf);
+  k_nvfp4_amax<RHT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, mask, ws, ts, nf, keep_from);
+}
+
+// First tile (32 B each) that the amax pass of a 1x16 quantisation loads
+// with the L2 evict-last policy: the last half-L2's worth of x, which the
+// encode pass then reads first (and with evict-first, releasing it).  The
+// 16x16 path reads x in the same order in both passes, so it marks nothing;
+// its weights usually fit in L2 whole.  The L2 size is read once per process.
+int64_t keep_from_of(int64_t ntiles, bool block_2d) {
+  static const int64_t l2 = [] {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+      v = 0;
+    return (int64_t)v;
+  }();
+  if (block_2d) return ntiles;
+  const int64_t keep = l2 / 2 / 32;
+  return ntiles > keep ? ntiles - keep : 0;
 }
 
 template <bool RHT, bool SR, bool DEQ>
@@ -363,8 +398,9 @@ MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, 
   uint16_t* dq = static_cast<uint16_t*>(dequant_bf16);
   const uint32_t mask = rht_sign_mask;
   const bool b2 = block_2d != 0, deq = dq != nullptr;
-  if (apply_rht) launch_amax<true>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, s);
-  else launch_amax<false>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, s);
+  const int64_t kf = keep_from_of(n / 16, block_2d != 0);
+  if (apply_rht) launch_amax<true>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, kf, s);
+  else launch_amax<false>(x, n / 16, mask, ws, d_tensor_scale, d_nonfinite, kf, s);
   if (apply_rht && stochastic)
     dispatch_deq<true, true>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
   else if (apply_rht)
