@@ -52,7 +52,7 @@ typedef int32_t mp_status;
 enum {
   MP_OK = 0,
   MP_EINVAL = -1,     /* null pointer, negative size, bad enum or hyperparameter */
-  MP_EALIGN = -2,     /* a tensor pointer is not 16-byte aligned */
+  MP_EALIGN = -2,     /* a pointer is misaligned (tensors 16-byte; see each call) */
   MP_ESHAPE = -3,     /* a shape the call does not take (see each call) */
   MP_EWORKSPACE = -4, /* workspace missing or smaller than required */
   MP_ECUDA = -5       /* a kernel launch failed */

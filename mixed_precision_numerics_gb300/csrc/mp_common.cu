@@ -10,13 +10,16 @@ static std::atomic<uint64_t> g_launches{0};
 void note_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 int sm_count() {
-  static int cached[64] = {0};
+  static std::atomic<int> cached[64];  // zero-initialised (static storage); 0 = not yet read
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) dev = 0;
-  if (dev < 64 && cached[dev] > 0) return cached[dev];
+  if (dev < 64) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  if (dev < 64) cached[dev] = n;
+  if (dev < 64) cached[dev].store(n, std::memory_order_relaxed);
   return n;
 }
 
@@ -28,8 +31,8 @@ MP_API const char* mp_status_str(mp_status s) {
   switch (s) {
     case MP_OK: return "ok";
     case MP_EINVAL: return "invalid argument (null pointer, negative size, bad dtype or hyperparameter)";
-    case MP_EALIGN: return "tensor pointer not 16-byte aligned";
-    case MP_ESHAPE: return "shape not supported (cols % 16 != 0, or rows % 16 != 0 for 16x16 blocks)";
+    case MP_EALIGN: return "pointer misaligned (tensors 16-byte, clipping workspace 8-byte)";
+    case MP_ESHAPE: return "shape not supported by the call (e.g. cols % 16 != 0, or cols % 32 != 0 for MX)";
     case MP_EWORKSPACE: return "workspace missing or too small";
     case MP_ECUDA: return "CUDA launch failed";
     default: return "unknown status";
