@@ -272,3 +272,18 @@ def test_cast_transpose_argument_errors():
     with pytest.raises(M.MpError) as e:
         M.fp8_cast_transpose_delayed(x, y, y, M.MP_E4M3, meta, hist)
     assert e.value.status == M.MP_ESHAPE
+
+
+def test_cast_transpose_of_an_empty_tensor_still_records_the_step():
+    """A [0, cols] cast is a step with amax 0: the ring slot is written and the
+    position advances, as for an empty fp8_cast_delayed."""
+    meta, hist = M.new_fp8_meta(), torch.full((3,), 5.0, device="cuda")
+    om, oh = O.new_fp8_meta(), np.full(3, 5.0, np.float32)
+    x = torch.empty((0, 32), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, dtype=torch.uint8, device="cuda")
+    for _ in range(4):
+        M.fp8_cast_transpose_delayed(x, y, y, M.MP_E4M3, meta, hist)
+        O.fp8_cast_delayed(np.zeros(0, np.uint16), O.BF16, O.E4M3, om, oh, 1.0)
+        torch.cuda.synchronize()
+        assert_meta_equal(M.read_fp8_meta(meta), om)
+        np.testing.assert_array_equal(hist.cpu().numpy().view(np.uint32), oh.view(np.uint32))

@@ -90,3 +90,12 @@ def test_shape_errors():
         with pytest.raises(M.MpError) as e:
             M.fp8_quantize_blockwise(x, y, sc, br, bc)
         assert e.value.status == M.MP_ESHAPE
+
+
+def test_empty_tensor_launches_nothing():
+    n0 = M.mp_launch_count()
+    for br in (1, 128):
+        x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+        M.fp8_quantize_blockwise(x, torch.empty(0, dtype=torch.uint8, device="cuda"),
+                                 torch.empty(0, device="cuda"), br, 128)
+    assert M.mp_launch_count() == n0

@@ -133,3 +133,17 @@ def test_most_recent_uses_only_the_latest_amax(fmt, fmax):
 def test_transpose_matches_numpy():
     y = np.random.default_rng(1).integers(0, 256, size=(48, 80)).astype(np.uint8)
     np.testing.assert_array_equal(O.transpose_u8(y), y.T)
+
+
+def test_positive_nan_byte_matches_torch_and_negative_nan_is_the_reading():
+    """Reading R1 maps every NaN to 0x7F.  For a positive NaN that is the byte
+    torch's float8 casts produce; torch keeps the sign of a negative NaN (0xFF),
+    where the reading here does not."""
+    import torch
+
+    x = np.array([np.nan, -np.nan], np.float32)
+    for fmt, dt in ((O.E4M3, torch.float8_e4m3fn), (O.E5M2, torch.float8_e5m2)):
+        lib = torch.from_numpy(x).to(dt).view(torch.uint8).numpy()
+        got = O.convert(x, O.F32, fmt)
+        assert got[0] == lib[0] == 0x7F
+        assert got[1] == 0x7F and lib[1] == 0xFF
