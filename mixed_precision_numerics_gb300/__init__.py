@@ -254,7 +254,8 @@ def mp_adamw_step(params, hp: AdamwHparams, state, grad_dtype: int | None = None
 
 def _marshal(params, grad_dtype, working_dtype):
     if isinstance(params, ctypes.Array):
-        assert grad_dtype is not None and working_dtype is not None
+        if grad_dtype is None or working_dtype is None:
+            raise ValueError("a prebuilt parameter array needs grad_dtype and working_dtype")
         return params, len(params), grad_dtype, working_dtype
     n = len(params)
     arr = make_param_array(params)
