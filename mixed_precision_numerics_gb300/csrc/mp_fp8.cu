@@ -8,10 +8,10 @@
 // k_fp8_cast: every thread streams 16 input elements per vector (32 B of
 // BF16/F16, 64 B of F32), 128 B of input in flight, and writes 16 output bytes
 // per vector, keeping a running NaN-propagating max |x| in a register.  CTAs
-// fold their amax into the meta word with one atomicMax each; CTA 0 folds the
-// history entries the call does not overwrite while the stream runs; the last
-// CTA to finish (atomic ticket, no waiting) writes the ring slot and derives
-// the next scale from the two maxima.
+// fold their amax into the meta word with one atomicMax each; every CTA first
+// folds a small slice of the history entries the call does not overwrite into
+// a second word; the last CTA to finish (atomic ticket, no waiting) writes the
+// ring slot and derives the next scale from the two maxima.
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -77,16 +77,18 @@ __device__ __forceinline__ uint32_t hist_key(float h) {
   return (h != h) ? 0x7FC00000u : (h > 0.0f ? __float_as_uint(h) : 0u);
 }
 
-// CTA 0, at the start of a history-max cast: fold the history entries this
-// call does not overwrite into meta->internal_hrest.
-__device__ __forceinline__ void fold_history_rest(mp_fp8_meta* meta, const float* hist, int32_t hist_len,
-                                                  int32_t slot, uint32_t* red) {
-  uint32_t hm = 0;
-  for (int i = threadIdx.x; i < hist_len; i += blockDim.x)
-    if (i != slot) hm = max(hm, hist_key(hist[i]));
-  hm = block_max_u32(hm, red);
-  if (threadIdx.x == 0) meta->internal_hrest = hm;
-  __syncthreads();  // red is reused
+// At the start of a history-max cast every CTA folds a strided slice of the
+// history entries this call does not overwrite (entries blockIdx.x + k *
+// gridDim.x) into meta->internal_hrest with atomicMax: a few loads per CTA, no
+// barrier, so no CTA starts its stream late.  The last CTA reads and clears it.
+__device__ __forceinline__ void fold_history_slice(mp_fp8_meta* meta, const float* hist, int32_t hist_len,
+                                                   int32_t slot) {
+  for (int64_t i = blockIdx.x + (int64_t)threadIdx.x * gridDim.x; i < hist_len;
+       i += (int64_t)blockDim.x * gridDim.x) {
+    if (i == slot) continue;
+    const uint32_t k = hist_key(hist[i]);
+    if (k) atomicMax(&meta->internal_hrest, k);
+  }
 }
 
 // End of every CTA: fold its amax into the meta word; the last CTA (atomic
@@ -105,7 +107,7 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
   if (!*is_last || threadIdx.x != 0) return;
   __threadfence();
   const uint32_t ab = atomicExch(&meta->internal_amax, 0u);
-  const uint32_t hm = algo == 1 ? ab : max(*reinterpret_cast<volatile uint32_t*>(&meta->internal_hrest), ab);
+  const uint32_t hm = algo == 1 ? ab : max(atomicExch(&meta->internal_hrest, 0u), ab);
   meta->internal_ticket = 0;
   const float amax = __uint_as_float(ab);
   meta->amax = amax;
@@ -165,7 +167,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
   __shared__ int is_last;
   const float scale = meta->scale;
   const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
-  if (blockIdx.x == 0 && algo == 0) fold_history_rest(meta, hist, hist_len, slot, red);
+  if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
 
   float acc = 0.0f;
   const int64_t nvec = n / kElems;
@@ -234,7 +236,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast_t(const void* __restrict_
   __shared__ __align__(16) uint8_t tile[kTT][kTT];
   const float scale = meta->scale;
   const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;
-  if (blockIdx.x == 0 && algo == 0) fold_history_rest(meta, hist, hist_len, slot, red);
+  if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
   const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
   const int lr = threadIdx.x >> 3, seg = (threadIdx.x & 7) * 16;  // row (pass 0) and column segment
   const int cw = threadIdx.x & 31, rs = (threadIdx.x >> 5) * 16;   // transposed: column group, row run

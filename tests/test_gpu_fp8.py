@@ -50,7 +50,7 @@ def assert_meta_equal(g: "M.Fp8Meta", o: "O.Fp8Meta"):
     assert f(g.scale_inv) == f(o.scale_inv)
     assert f(g.amax) == f(o.amax), (g.amax, o.amax)
     assert g.pos == o.pos
-    assert g.internal_amax == 0 and g.internal_ticket == 0
+    assert g.internal_amax == 0 and g.internal_ticket == 0 and g.internal_hrest == 0
 
 
 @pytest.mark.parametrize("fmt", [M.MP_E4M3, M.MP_E5M2])
