@@ -447,6 +447,21 @@ class Workload:
         ]
         self.copy_stream = torch.cuda.Stream()
 
+    def h2d_link_gbs(self) -> float:
+        """Host-to-device bandwidth of this machine: one 1 GiB pinned copy, best of 3."""
+        torch = self.torch
+        h = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+        d = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+        best = 0.0
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            d.copy_(h, non_blocking=True)
+            b.record()
+            torch.cuda.synchronize()
+            best = max(best, (1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9)
+        return best
+
     def e2e_copy_in(self, k: int, copied, free):
         """On the copy stream: step k's inputs into device set k % 2, once the
         step that last read that set is done."""
@@ -780,8 +795,11 @@ def main():
             b.record(stream)
             torch.cuda.synchronize()
             e_gbs, e_ms = job_gbs(args.steps * wl.step_bytes, a.elapsed_time(b), world)
+            link = wl.h2d_link_gbs()
             e2e = {"value": round(e_gbs, 1), "unit": UNIT, "ms_per_step": round(e_ms / args.steps, 3),
                    "h2d_bytes_per_step": int(wl.h2d), "d2h_bytes_per_step": int(wl.d2h),
+                   "h2d_link_gbs": round(link, 1),
+                   "h2d_ms_per_step_at_link_speed": round(wl.h2d / (link * 1e9) * 1e3, 2),
                    "api": "mp_adamw_step + loss_scale_update + fp8_cast_delayed x2 + nvfp4_quantize x3 "
                           "with pinned host inputs copied in and outputs copied out every step; step k+1's "
                           "inputs are copied (second stream, second device input set) while step k runs"}
