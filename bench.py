@@ -57,6 +57,9 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle baseline")
     p.add_argument("--small", action="store_true",
                    help="profiling case: optimizer over decoder layer 0 only (218M params), 2 FP8 inputs")
+    p.add_argument("--trace", metavar="PATH",
+                   help="write one JSON line per timed step (loss scale, skip count, FP8 amax/scale, NVFP4 tensor "
+                        "scales, per-call ms) to PATH; adds a few small device-to-host copies per step")
     return p.parse_args()
 
 
@@ -318,6 +321,36 @@ class Workload:
             M.nvfp4_quantize(q["x"], q["codes"], q["scales"], q["ts"], q["nf"], q["ws"], block_2d=q["b2"],
                              stochastic=q["sr"], seed=q["seed"], apply_rht=q["rht"], sign_mask=q["mask"])
             rec(6 + i)
+
+    # ---- per-step trace (optional) ---------------------------------------------------------
+    def trace_buffers(self, steps: int):
+        """Pinned host rows, one per step: scaler state, both FP8 metas, and the
+        tensor scale and flag of each NVFP4 call."""
+        torch = self.torch
+        return {"state": torch.empty((steps, 88), dtype=torch.uint8, pin_memory=True),
+                "meta": torch.empty((steps, 2, 32), dtype=torch.uint8, pin_memory=True),
+                "ts": torch.empty((steps, len(self.q)), dtype=torch.float32, pin_memory=True),
+                "nf": torch.empty((steps, len(self.q)), dtype=torch.int32, pin_memory=True)}
+
+    def trace_copy(self, tr, k: int):
+        """Stream-ordered copies of step k's state into row k (no synchronisation)."""
+        tr["state"][k].copy_(self.state, non_blocking=True)
+        tr["meta"][k, 0].copy_(self.meta_act, non_blocking=True)
+        tr["meta"][k, 1].copy_(self.meta_grd, non_blocking=True)
+        for i, q in enumerate(self.q):
+            tr["ts"][k, i].copy_(q["ts"][0], non_blocking=True)
+            tr["nf"][k, i].copy_(q["nf"][0], non_blocking=True)
+
+    def trace_record(self, tr, k: int) -> dict:
+        M = self.M
+        st = M.ScalerState.from_buffer_copy(tr["state"][k].numpy().tobytes())
+        metas = [M.Fp8Meta.from_buffer_copy(tr["meta"][k, j].numpy().tobytes()) for j in range(2)]
+        return {"loss_scale": st.scale, "found_inf": st.found_inf, "skipped": st.skipped, "applied_steps": st.step,
+                "growth_tracker": st.growth_tracker,
+                "fp8": {name: {"amax": m.amax, "next_scale": m.scale, "pos": m.pos}
+                        for name, m in zip(("act_e4m3", "grad_e5m2"), metas)},
+                "nvfp4": {q["name"]: {"tensor_scale": float(tr["ts"][k, i]), "nonfinite": int(tr["nf"][k, i])}
+                          for i, q in enumerate(self.q)}}
 
     def clipped_check_ms(self, reps: int = 5) -> float:
         """The check pass with gradient-norm clipping (max norm 1.0) on the same
@@ -731,9 +764,12 @@ def main():
     launches0 = M.mp_launch_count()
     t_start = torch.cuda.Event(enable_timing=True)
     t_stop = torch.cuda.Event(enable_timing=True)
+    trace = wl.trace_buffers(args.steps) if args.trace else None
     t_start.record(stream)
     for k in range(args.steps):
         wl.step(args.warmup + k, evs[k])
+        if trace is not None:
+            wl.trace_copy(trace, k)
     t_stop.record(stream)
     torch.cuda.synchronize()
     launches = M.mp_launch_count() - launches0
@@ -743,6 +779,13 @@ def main():
 
     per_call_ms = {name: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(args.steps))
                    for i, name in enumerate(wl.calls)}
+    if trace is not None and rank == 0:
+        with open(args.trace, "w") as fh:
+            for k in range(args.steps):
+                rec = wl.trace_record(trace, k)
+                rec["step"] = args.warmup + k
+                rec["ms"] = {name: round(evs[k][i].elapsed_time(evs[k][i + 1]), 4) for i, name in enumerate(wl.calls)}
+                fh.write(json.dumps(rec) + "\n")
     peak, peak_kind = hbm_peak()
     kernels = {}
     for name in wl.calls:
