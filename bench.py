@@ -495,6 +495,24 @@ class Workload:
             best = max(best, (1 << 30) / (a.elapsed_time(b) * 1e-3) / 1e9)
         return best
 
+    def e2e_copy_only_ms(self, reps: int = 3) -> float:
+        """Milliseconds to copy one step's inputs in, with no kernels running:
+        the floor of the pipelined end-to-end step on this machine."""
+        torch = self.torch
+        cur = torch.cuda.current_stream()
+        copied = [torch.cuda.Event() for _ in range(2)]
+        free = [torch.cuda.Event() for _ in range(2)]
+        for e in free:
+            e.record(cur)
+        self.copy_stream.wait_stream(cur)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(self.copy_stream)
+        for k in range(reps):
+            self.e2e_copy_in(k, copied, free)
+        b.record(self.copy_stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
     def e2e_copy_in(self, k: int, copied, free):
         """On the copy stream: step k's inputs into device set k % 2, once the
         step that last read that set is done."""
@@ -839,10 +857,12 @@ def main():
             torch.cuda.synchronize()
             e_gbs, e_ms = job_gbs(args.steps * wl.step_bytes, a.elapsed_time(b), world)
             link = wl.h2d_link_gbs()
+            copy_ms = wl.e2e_copy_only_ms()
             e2e = {"value": round(e_gbs, 1), "unit": UNIT, "ms_per_step": round(e_ms / args.steps, 3),
                    "h2d_bytes_per_step": int(wl.h2d), "d2h_bytes_per_step": int(wl.d2h),
                    "h2d_link_gbs": round(link, 1),
                    "h2d_ms_per_step_at_link_speed": round(wl.h2d / (link * 1e9) * 1e3, 2),
+                   "h2d_ms_per_step_measured": round(copy_ms, 2),
                    "api": "mp_adamw_step + loss_scale_update + fp8_cast_delayed x2 + nvfp4_quantize x3 "
                           "with pinned host inputs copied in and outputs copied out every step; step k+1's "
                           "inputs are copied (second stream, second device input set) while step k runs"}
