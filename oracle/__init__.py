@@ -122,6 +122,7 @@ def lib() -> ctypes.CDLL:
             "orc_transpose_u8": (None, [P, I64, I64, P]),
             "orc_fp8_quantize_blockwise": (None, [P, ctypes.c_int, I64, I64, I32, I32, ctypes.c_int, P, P]),
             "orc_mx_quantize": (None, [P, ctypes.c_int, I64, I64, ctypes.c_int, P, P, P]),
+            "orc_fp8_saturation_count": (I64, [P, ctypes.c_int, I64, ctypes.c_int, ctypes.c_float]),
             "orc_nvfp4_prepare": (ctypes.c_int, [P, I64, I64, ctypes.c_int, U16, P]),
             "orc_nvfp4_tensor_scale": (F, [F, P]),
             "orc_nvfp4_encode_rows": (
@@ -248,6 +249,11 @@ def fp8_cast_array(x: np.ndarray, x_fmt: int, fmt: int, scale: float) -> np.ndar
     y = np.empty(x.shape, dtype=np.uint8)
     lib().orc_fp8_cast_array(_p(x), x_fmt, x.size, _p(y), fmt, np.float32(scale))
     return y
+
+
+def fp8_saturation_count(x: np.ndarray, x_fmt: int, fmt: int, scale: float) -> int:
+    x = np.ascontiguousarray(x, dtype=_NP[x_fmt])
+    return int(lib().orc_fp8_saturation_count(_p(x), x_fmt, x.size, fmt, np.float32(scale)))
 
 
 AMAX_HISTORY_MAX, AMAX_MOST_RECENT = 0, 1

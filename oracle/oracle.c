@@ -469,6 +469,18 @@ void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt
   for (int64_t i = 0; i < n; ++i) y[i] = orc_fp8_cast_one(load_f32(x, x_fmt, i), scale, fmt);
 }
 
+int64_t orc_fp8_saturation_count(const void* x, int x_fmt, int64_t n, int fmt, float scale) {
+  int M, emin, bias;
+  double maxv;
+  fp8_params(fmt, &M, &emin, &bias, &maxv);
+  int64_t c = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    float p = load_f32(x, x_fmt, i) * scale;
+    if (fabs((double)p) > maxv) ++c; /* false for NaN */
+  }
+  return c;
+}
+
 void orc_fp8_history_update(orc_fp8_meta* meta, float* history, int32_t hist_len, float margin,
                             float amax, int fmt, int amax_algo) {
   meta->amax = amax;

@@ -150,6 +150,11 @@ typedef struct {
 uint8_t orc_fp8_cast_one(float x, float scale, int fmt);
 /* Casts n elements with meta->scale; does not touch meta. */
 void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt, float scale);
+/* Elements the cast saturates ([FP8-TE] "Delayed Scaling 동작 원리": margin is
+ * raised when FP8's range is under-used and lowered when casts saturate):
+ * the count of i with |fp32(x_i) * scale| (binary32 product) above the
+ * format's largest finite value, infinities included, NaN not counted. */
+int64_t orc_fp8_saturation_count(const void* x, int x_fmt, int64_t n, int fmt, float scale);
 /* Records amax in the ring and derives the next scale from max(history)
  * (amax_algo 0) or from this amax alone (amax_algo 1, "most_recent",
  * [FP8-TE] "도입 체크리스트"). */

@@ -147,3 +147,18 @@ def test_positive_nan_byte_matches_torch_and_negative_nan_is_the_reading():
         got = O.convert(x, O.F32, fmt)
         assert got[0] == lib[0] == 0x7F
         assert got[1] == 0x7F and lib[1] == 0xFF
+
+
+@pytest.mark.parametrize("fmt,fmax", [(O.E4M3, 448.0), (O.E5M2, 57344.0)])
+def test_saturation_count_closed_form(fmt, fmax):
+    """Integers 0..9999 at scale s: exactly those with k * s > fmax saturate
+    (the products are exact here), infinities count, NaN does not; the count
+    equals the number of saturated bytes in the cast."""
+    k = np.arange(10000, dtype=np.float32)
+    for s in (0.5, 1.0, 7.0):  # k * s exact in binary32: k > fmax / s saturates
+        assert O.fp8_saturation_count(k, O.F32, fmt, s) == max(0, 9999 - int(np.floor(fmax / s)))
+    x = np.array([np.inf, -np.inf, np.nan, 1.0, -1e9], np.float32)
+    assert O.fp8_saturation_count(x, O.F32, fmt, 1.0) == 3
+    y = O.fp8_cast_array(x[[0, 1, 3, 4]], O.F32, fmt, 1.0)
+    maxcode = 0x7E if fmt == O.E4M3 else 0x7B
+    assert int(np.sum((y & 0x7F) == maxcode)) == 3
