@@ -225,6 +225,19 @@ MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, vo
                                   mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
                                   int32_t history_len, float margin, int32_t amax_algo, void* stream);
 
+/* fp8_cast_delayed_count — fp8_cast_delayed that also adds to *d_saturated
+ * the number of elements the cast saturates: |fp32(x) * scale| (binary32
+ * product) above fp8_max, infinities included, NaN not counted ([FP8-TE]
+ * "Delayed Scaling 동작 원리": margin is tuned against saturation).  Same
+ * outputs and state updates as fp8_cast_delayed; the counter accumulates over
+ * calls (the caller zeroes it); d_saturated is a device pointer, 8-byte
+ * aligned.  A separate entry point so that the plain cast pays no atomics.
+ * One kernel launch. */
+MP_API mp_status fp8_cast_delayed_count(const void* x, mp_dtype x_dtype, int64_t n, void* y,
+                                        mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
+                                        int32_t history_len, float margin, int32_t amax_algo,
+                                        unsigned long long* d_saturated, void* stream);
+
 /* fp8_cast_transpose_delayed — fp8_cast_delayed of a [rows, cols] tensor that
  * also writes y_t [cols, rows] = transpose(y) from the same single read: the
  * backward GEMMs use the transposed operand ([NVFP4] §2.2 item 3 on the

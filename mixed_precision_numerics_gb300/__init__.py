@@ -102,6 +102,7 @@ def _load() -> ctypes.CDLL:
         "loss_scale_update": (I32, [P, P, P]),
         "fp8_cast_delayed": (I32, [P, I32, I64, P, I32, P, P, I32, F, I32, P]),
         "fp8_cast_transpose_delayed": (I32, [P, I32, I64, I64, P, P, I32, P, P, I32, F, I32, P]),
+        "fp8_cast_delayed_count": (I32, [P, I32, I64, P, I32, P, P, I32, F, I32, P, P]),
         "fp8_quantize_blockwise": (I32, [P, I32, I64, I64, I32, I32, P, I32, P, P]),
         "nvfp4_workspace_size": (S, []),
         "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
@@ -295,6 +296,16 @@ def fp8_cast_delayed(x, y, fp8_dtype: int, meta, history, margin: float = 1.0, s
                                 _stream(stream)))
 
 
+def fp8_cast_delayed_count(x, y, fp8_dtype: int, meta, history, saturated, margin: float = 1.0,
+                           amax_algo: int = MP_AMAX_HISTORY_MAX, stream=None) -> None:
+    """fp8_cast_delayed that also adds the number of saturated elements to
+    `saturated` (an int64 device tensor of one element)."""
+    _check("fp8_cast_delayed_count",
+           lib.fp8_cast_delayed_count(_ptr(x), _dtype_code(x), x.numel(), _ptr(y), fp8_dtype, _ptr(meta),
+                                      _ptr(history), history.numel(), float(margin), amax_algo, _ptr(saturated),
+                                      _stream(stream)))
+
+
 def fp8_cast_transpose_delayed(x, y, y_t, fp8_dtype: int, meta, history, margin: float = 1.0,
                                amax_algo: int = MP_AMAX_HISTORY_MAX, stream=None) -> None:
     """x: [rows, cols]; y: rows*cols bytes; y_t: cols*rows bytes (the transpose)."""
@@ -357,7 +368,7 @@ __all__ = [
     "AdamwHparams", "Fp8Meta", "MpError", "MpParam", "Param", "ScalerCfg", "ScalerState",
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2", "MP_E2M1", "MP_E2M3", "MP_E3M2", "mx_quantize",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
-    "fp8_cast_transpose_delayed", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
+    "fp8_cast_transpose_delayed", "fp8_cast_delayed_count", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",

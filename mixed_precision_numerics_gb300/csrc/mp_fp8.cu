@@ -131,7 +131,9 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
 // product (a NaN input, or an infinite input times a zero multiplier) gives
 // 0x7F; the products are checked, not the inputs.
 template <int XT, bool E5M2>
-__device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out) {
+__device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out,
+                                        uint32_t* saturated = nullptr) {
+  constexpr float fmax = E5M2 ? 57344.0f : 448.0f;
   float vmax = 0.0f, pmax = 0.0f;
   uint32_t h[8];
 #pragma unroll
@@ -142,6 +144,7 @@ __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, floa
     const float p0 = __fmul_rn(f.x, scale), p1 = __fmul_rn(f.y, scale);
     pmax = max_abs_nan(pmax, p0);
     pmax = max_abs_nan(pmax, p1);
+    if (saturated) *saturated += (fabsf(p0) > fmax) + (fabsf(p1) > fmax);  // NaN compares false
     h[k] = cast_pair<E5M2>(p0, p1);
   }
   uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
@@ -158,10 +161,11 @@ __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, floa
   return o;
 }
 
-template <int XT, bool E5M2>
+template <int XT, bool E5M2, bool COUNT>
 __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ x, int64_t n,
                                                        uint8_t* __restrict__ y, mp_fp8_meta* meta,
-                                                       float* hist, int32_t hist_len, float margin, int32_t algo) {
+                                                       float* hist, int32_t hist_len, float margin, int32_t algo,
+                                                       unsigned long long* saturated_out) {
   constexpr int U = unroll_of<XT>();
   __shared__ uint32_t red[32];
   __shared__ int is_last;
@@ -170,6 +174,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
   if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
 
   float acc = 0.0f;
+  uint32_t sat = 0;  // saturated elements (COUNT only)
   const int64_t nvec = n / kElems;
   const int64_t step = (int64_t)gridDim.x * kThreads * U;
   for (int64_t v0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; v0 < nvec; v0 += step) {
@@ -184,7 +189,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
       const int64_t vec = v0 + (int64_t)u * kThreads;
       if (vec >= nvec) continue;
       float vmax;
-      st_cs(y + vec * kElems, cast16<XT, E5M2>(raw[u], scale, &vmax));
+      st_cs(y + vec * kElems, cast16<XT, E5M2>(raw[u], scale, &vmax, COUNT ? &sat : nullptr));
       acc = max_abs_nan(acc, vmax);
     }
   }
@@ -198,7 +203,13 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
       uint32_t b = cast_pair<E5M2>(p, 0.0f) & 0xFFu;
       if (p != p) b = 0x7F;
       y[i] = (uint8_t)b;
+      if (COUNT) sat += fabsf(p) > (E5M2 ? 57344.0f : 448.0f);
     }
+  }
+  if (COUNT) {
+#pragma unroll
+    for (int h = 16; h >= 1; h >>= 1) sat += __shfl_xor_sync(0xFFFFFFFFu, sat, h);
+    if ((threadIdx.x & 31) == 0 && sat) atomicAdd(saturated_out, (unsigned long long)sat);
   }
   fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
 }
@@ -407,17 +418,19 @@ int occ_of(K kernel) {
   return o;
 }
 
-template <int XT, bool E5M2>
+template <int XT, bool E5M2, bool COUNT>
 mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float* hist, int32_t len,
-                 float margin, int32_t algo, cudaStream_t s) {
-  static const int occ = occ_of(k_fp8_cast<XT, E5M2>);
+                 float margin, int32_t algo, unsigned long long* saturated, cudaStream_t s) {
+  static const int occ = occ_of(k_fp8_cast<XT, E5M2, COUNT>);
   const int64_t nvec = n / kElems;
   constexpr int U = unroll_of<XT>();
   const int64_t ctas = (nvec + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
-  k_fp8_cast<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin, algo);
+  k_fp8_cast<XT, E5M2, COUNT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin, algo,
+                                                                       saturated);
   note_launches(1);
   return launch_status();
 }
+
 
 template <int XT, bool E5M2>
 mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_t* y_t, mp_fp8_meta* meta,
@@ -459,13 +472,10 @@ mp_status check_common(mp_dtype x_dtype, mp_dtype fp8_dtype, const mp_fp8_meta* 
   return MP_OK;
 }
 
-}  // namespace
-}  // namespace mp
-
-extern "C" MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
-                                             mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
-                                             int32_t history_len, float margin, int32_t amax_algo, void* stream) {
-  using namespace mp;
+template <bool COUNT>
+mp_status cast_entry(const void* x, mp_dtype x_dtype, int64_t n, void* y, mp_dtype fp8_dtype, mp_fp8_meta* d_meta,
+                     float* d_history, int32_t history_len, float margin, int32_t amax_algo,
+                     unsigned long long* saturated, void* stream) {
   if (n < 0 || (n > 0 && (!x || !y))) return MP_EINVAL;
   const mp_status rc = check_common(x_dtype, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo);
   if (rc != MP_OK) return rc;
@@ -475,15 +485,35 @@ extern "C" MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, in
   const bool e5 = fp8_dtype == MP_E5M2;
   switch (x_dtype) {
     case MP_F32:
-      return e5 ? launch<XF32, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
-                : launch<XF32, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
+      return e5 ? launch<XF32, true, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated, s)
+                : launch<XF32, false, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated, s);
     case MP_F16:
-      return e5 ? launch<XF16, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
-                : launch<XF16, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
+      return e5 ? launch<XF16, true, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated, s)
+                : launch<XF16, false, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated, s);
     default:
-      return e5 ? launch<XBF16, true>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s)
-                : launch<XBF16, false>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, s);
+      return e5 ? launch<XBF16, true, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated, s)
+                : launch<XBF16, false, COUNT>(x, n, yb, d_meta, d_history, history_len, margin, amax_algo, saturated,
+                                              s);
   }
+}
+
+}  // namespace
+}  // namespace mp
+
+extern "C" MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
+                                             mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
+                                             int32_t history_len, float margin, int32_t amax_algo, void* stream) {
+  return mp::cast_entry<false>(x, x_dtype, n, y, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo,
+                               nullptr, stream);
+}
+
+extern "C" MP_API mp_status fp8_cast_delayed_count(const void* x, mp_dtype x_dtype, int64_t n, void* y,
+                                                   mp_dtype fp8_dtype, mp_fp8_meta* d_meta, float* d_history,
+                                                   int32_t history_len, float margin, int32_t amax_algo,
+                                                   unsigned long long* d_saturated, void* stream) {
+  if (!d_saturated || (reinterpret_cast<uintptr_t>(d_saturated) & 7u)) return d_saturated ? MP_EALIGN : MP_EINVAL;
+  return mp::cast_entry<true>(x, x_dtype, n, y, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo,
+                              d_saturated, stream);
 }
 
 extern "C" MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,

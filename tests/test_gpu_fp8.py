@@ -287,3 +287,31 @@ def test_cast_transpose_of_an_empty_tensor_still_records_the_step():
         torch.cuda.synchronize()
         assert_meta_equal(M.read_fp8_meta(meta), om)
         np.testing.assert_array_equal(hist.cpu().numpy().view(np.uint32), oh.view(np.uint32))
+
+
+@pytest.mark.parametrize("fmt", [M.MP_E4M3, M.MP_E5M2])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_saturation_count_matches_the_oracle(fmt, dtype):
+    """The counting cast writes the same bytes and state as the plain one and
+    adds the oracle's saturation count; the counter accumulates over calls."""
+    n = 1_000_003
+    xf = synth.fill(synth.recipe(70, 1, 1.0, 0.01, 800.0, synth.OUT_T3), synth.F32, n)
+    xf[[3, 5, 7]] = [np.inf, -np.inf, np.nan]
+    x = xf if dtype == torch.float32 else O.convert(xf, O.F32, XFMT[dtype])
+    xt = to_dev(x) if dtype == torch.float32 else to_dev(x, dtype)
+    sat = torch.zeros(1, dtype=torch.int64, device="cuda")
+    total = 0
+    for scale in (1.0, 0.25, 40.0):
+        m1, m2 = M.new_fp8_meta(), M.new_fp8_meta()
+        set_meta(m1, scale)
+        set_meta(m2, scale)
+        h1, h2 = torch.zeros(4, device="cuda"), torch.zeros(4, device="cuda")
+        y1 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        y2 = torch.empty(n, dtype=torch.uint8, device="cuda")
+        M.fp8_cast_delayed(xt, y1, fmt, m1, h1)
+        M.fp8_cast_delayed_count(xt, y2, fmt, m2, h2, sat)
+        torch.cuda.synchronize()
+        assert torch.equal(y1, y2) and torch.equal(m1, m2)
+        assert torch.equal(h1.view(torch.int32), h2.view(torch.int32))  # bits: the amax may be NaN
+        total += O.fp8_saturation_count(x, XFMT[dtype], FMT[fmt], scale)
+        assert int(sat.item()) == total

@@ -81,6 +81,10 @@ def test_argument_validation_without_gpu(M):
     assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 0.0, 0, None) == M.MP_EINVAL
     assert L.fp8_cast_delayed(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 2, None) == M.MP_EINVAL
     assert L.fp8_cast_delayed(8, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_EALIGN
+    c = L.fp8_cast_delayed_count
+    assert c(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, None, None) == M.MP_EINVAL
+    assert c(16, M.MP_BF16, 10, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, 12, None) == M.MP_EALIGN
+    assert c(16, M.MP_BF16, 10, 16, M.MP_F16, 16, 16, 4, 1.0, 0, 16, None) == M.MP_EINVAL
     b = L.fp8_quantize_blockwise
     assert b(16, M.MP_BF16, 4, 128, 64, 64, 16, M.MP_E4M3, 16, None) == M.MP_ESHAPE
     assert b(16, M.MP_BF16, 4, 120, 1, 128, 16, M.MP_E4M3, 16, None) == M.MP_ESHAPE
