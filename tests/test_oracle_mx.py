@@ -134,3 +134,23 @@ def test_nvfp4_blocks_are_finer_than_mxfp4():
     e_mx = np.mean((O.convert(dq_mx, O.BF16, O.F32) - xf) ** 2)
     e_nv = np.mean((O.convert(dq_nv, O.BF16, O.F32) - xf) ** 2)
     assert e_nv < e_mx
+
+
+def test_block_sizes_and_scale_kinds_printed_on_the_pages():
+    g = golden("mx_format.json")
+    rng = np.random.default_rng(11)
+    x = bf16(rng.standard_normal((4, 256)) * 5)
+    _, scales, dq = O.mx_quantize(x, O.BF16, O.E2M1)
+    assert scales.shape == (4, 256 // g["mx_block"])
+    # every MX scale is a power of two: its dequantised element values divide
+    # by 2^(byte - 127) into E2M1 magnitudes
+    mags = set(golden("nvfp4_format.json")["e2m1_magnitudes"])
+    dqf = O.convert(dq, O.BF16, O.F32).reshape(4, -1, g["mx_block"])
+    for r in range(4):
+        for b in range(scales.shape[1]):
+            unit = 2.0 ** (int(scales[r, b]) - 127)
+            assert set(np.abs(dqf[r, b]) / unit) <= mags
+    # NVFP4 keeps one E4M3 scale per 16 elements: twice as many scales
+    _, nv_scales, _, _, _ = O.nvfp4_quantize(x, False, False, 0, False, 0)
+    assert nv_scales.shape == (4, 256 // g["nvfp4_block"])
+    assert nv_scales.size == 2 * scales.size
