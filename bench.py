@@ -300,6 +300,7 @@ class Workload:
         self.units["fp8_act_e4m3_with_transpose"] = self.units["fp8_blockwise_1x128_act"] = self.fp8_n
         self.units["fp8_blockwise_128x128_w"] = r.w_rows * r.w_cols
         self.units["mxfp4_act"] = self.units["mxfp8_e4m3_act"] = self.units["mxfp6_e2m3_act"] = r.act_rows * r.act_cols
+        self.units["rht16_bf16_grad"] = g4.rows * g4.cols
 
     def step(self, k: int, ev=None):
         """Enqueue one step on the current stream; ev: list of len(calls)+1 events."""
@@ -423,6 +424,11 @@ class Workload:
         self.extra_bytes["mxfp8_e4m3_act"] = (3.0 + 1.0 / 32) * n_a
         calls["mxfp6_e2m3_act"] = lambda k: M.mx_quantize(pick(ar, k), pick(mx_c, k), pick(mx_s, k), M.MP_E2M3)
         self.extra_bytes["mxfp6_e2m3_act"] = (3.0 + 1.0 / 32) * n_a  # one FP6 code per byte
+        gq = self.q[2]
+        gr = xs[gq["name"]]
+        ry = rot(torch.empty_like(gq["x"]), clone=False)
+        calls["rht16_bf16_grad"] = lambda k: M.rht16(pick(gr, k), pick(ry, k), gq["mask"])
+        self.extra_bytes["rht16_bf16_grad"] = 4.0 * gq["rows"] * gq["cols"]  # read 2, write 2
         for q in self.q:
             qc, qs = rot(q["codes"], clone=False), rot(q["scales"], clone=False)
             calls[q["name"]] = (lambda q, xr, qc, qs: lambda k: M.nvfp4_quantize(
