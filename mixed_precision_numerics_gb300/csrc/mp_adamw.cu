@@ -23,6 +23,10 @@
 //                   measurements on the full Llama-3-8B list, larger or
 //                   smaller amounts in flight, and power-of-two chunk sizes,
 //                   were slower.
+// With gradient-norm clipping the check pass is k_check_finite_clip, which
+// also writes one binary32 sum of the squared unscaled grads per 16384-element
+// tile, and k_clip_finish folds those sums in binary64 (32 one-warp CTAs and a
+// last-CTA fold) into the norm and the clip factor the update multiplies by.
 // The table of tensors travels as a __grid_constant__ kernel parameter (up to
 // 512 tensors per launch), so no device-side copy or allocation is needed.
 #include <new>
