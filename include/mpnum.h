@@ -212,7 +212,8 @@ enum { MP_AMAX_HISTORY_MAX = 0, MP_AMAX_MOST_RECENT = 1 };
  * Reads x once.  For each of the n elements of x (x_dtype MP_F32, MP_F16 or
  * MP_BF16): y = saturate(round-to-nearest-even(fp32(x) * d_meta->scale)) in
  * fp8_dtype (MP_E4M3: max 448; MP_E5M2: max 57344); magnitudes beyond the
- * maximum, infinities included, become the signed maximum; NaN becomes 0x7F.
+ * maximum, infinities included, become the signed maximum; a NaN product
+ * becomes 0x7F with the input element's sign bit (0xFF when it is negative).
  * In the same pass amax = max |x| (NaN if any element is NaN).  Then
  * d_meta->amax = amax, d_history[p] = amax with p = pos mod history_len,
  * pos = (p + 1) % history_len, and if H = max(d_history) (amax_algo
@@ -258,7 +259,8 @@ MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int
  * for a block holding a NaN; FP32, row-major
  * [ceil(rows/br)][ceil(cols/bc)]), and every element
  * y = saturate(RNE(fp32(x) * r)) with r = fp8_max / amax if amax is finite
- * and > 0, else r = 0 (a NaN product gives 0x7F).  Each block is read once.
+ * and > 0, else r = 0 (a NaN product gives 0x7F or, for a negative input
+ * element, 0xFF).  Each block is read once.
  * cols % 16 == 0; x, y 16-byte aligned.  One kernel launch. */
 MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
                                         int32_t block_rows, int32_t block_cols, void* y, mp_dtype fp8_dtype,

@@ -92,7 +92,8 @@ float orc_bf16_to_f32(uint16_t h) {
  * E5M2: bias 15, exponent 11111 is inf/NaN as in IEEE, so the largest finite
  * value is 1.75 * 2^15 = 57344 (derived from the layout; not printed).
  * The cast clips (x_fp8 = clip(x/s, -448, 448) on [FP8-TE]); reading R1:
- * infinities clip too, and NaN maps to 0x7F. */
+ * infinities clip too, and NaN maps to S.1111111 (0x7F / 0xFF) with the sign
+ * of the NaN (of the input element when the NaN comes from the product). */
 static void fp8_params(int fmt, int* M, int* emin, int* bias, double* maxv) {
   if (fmt == ORC_E4M3) { *M = 3; *emin = -6; *bias = 7; *maxv = 448.0; }
   else { *M = 2; *emin = -14; *bias = 15; *maxv = 57344.0; }
@@ -102,8 +103,8 @@ uint8_t orc_f32_to_fp8_sat(float x, int fmt) {
   int M, emin, bias;
   double maxv;
   fp8_params(fmt, &M, &emin, &bias, &maxv);
-  if (isnan(x)) return 0x7F;
   uint8_t s = signbit(x) ? 0x80 : 0;
+  if (isnan(x)) return s | 0x7F;
   double a = isinf(x) ? maxv : fabs((double)x);
   double r = round_mag(a, M, emin);
   if (r > maxv) r = maxv;
@@ -462,7 +463,12 @@ void orc_loss_scale_update(orc_scaler_state* st, const orc_scaler_cfg* cfg) {
  * finite positive number, leaves the scale unchanged.
  * ------------------------------------------------------------------------- */
 uint8_t orc_fp8_cast_one(float x, float scale, int fmt) {
-  return orc_f32_to_fp8_sat(x * scale, fmt);
+  const float p = x * scale;
+  /* reading R1: a NaN product (a NaN input, or an infinity times a zero
+   * multiplier) takes the input element's sign; the sign of a NaN an
+   * operation creates is not fixed across machines */
+  if (isnan(p)) return (signbit(x) ? 0x80 : 0) | 0x7F;
+  return orc_f32_to_fp8_sat(p, fmt);
 }
 
 void orc_fp8_cast_array(const void* x, int x_fmt, int64_t n, uint8_t* y, int fmt, float scale) {
@@ -542,7 +548,7 @@ void orc_fp8_quantize_blockwise(const void* x, int x_fmt, int64_t rows, int64_t 
       float rr = (isfinite(amax) && amax > 0.0f) ? fp8_max / amax : 0.0f;
       for (int64_t r = br * block_rows; r < r1; ++r)
         for (int64_t c = bc * block_cols; c < c1; ++c)
-          y[r * cols + c] = orc_f32_to_fp8_sat(load_f32(x, x_fmt, r * cols + c) * rr, fmt);
+          y[r * cols + c] = orc_fp8_cast_one(load_f32(x, x_fmt, r * cols + c), rr, fmt);
     }
   }
 }

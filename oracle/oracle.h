@@ -20,9 +20,10 @@
  * Parity pins: every function here is pinned by the CPU test suite against
  * values the pages print, closed forms, brute-force searches or independent
  * library routines.  Philox4x32-10 is pinned against an independent library
- * implementation of the same generator.  The NaN byte choices (R1, R-NaN16)
- * are readings with no page value behind them: parity unpinned for those
- * bytes beyond self-consistency.
+ * implementation of the same generator.  The FP8 NaN byte (R1) has no page
+ * value behind it and is pinned to torch's float8 casts (both signs); the
+ * 16-bit NaN pattern (R-NaN16) is a reading with no page or agreed library
+ * value behind it: parity unpinned for that pattern beyond self-consistency.
  */
 #ifndef MPNUM_ORACLE_H
 #define MPNUM_ORACLE_H
@@ -47,7 +48,8 @@ uint16_t orc_f32_to_f16(float x);   /* overflow -> inf; NaN -> 0x7FFF */
 float orc_f16_to_f32(uint16_t h);
 uint16_t orc_f32_to_bf16(float x);  /* overflow -> inf; NaN -> 0x7FFF */
 float orc_bf16_to_f32(uint16_t h);
-/* Saturating FP8: |x| beyond max (inf included) -> ±max; NaN -> 0x7F. */
+/* Saturating FP8: |x| beyond max (inf included) -> ±max; NaN -> 0x7F with
+ * the NaN's sign bit (0xFF for a negative NaN). */
 uint8_t orc_f32_to_fp8_sat(float x, int fmt);
 float orc_fp8_to_f32(uint8_t c, int fmt);
 uint8_t orc_f32_to_e2m1(float x); /* finite x; |x| > 6 -> 6; sign kept on zero */

@@ -135,18 +135,19 @@ def test_transpose_matches_numpy():
     np.testing.assert_array_equal(O.transpose_u8(y), y.T)
 
 
-def test_positive_nan_byte_matches_torch_and_negative_nan_is_the_reading():
-    """Reading R1 maps every NaN to 0x7F.  For a positive NaN that is the byte
-    torch's float8 casts produce; torch keeps the sign of a negative NaN (0xFF),
-    where the reading here does not."""
+def test_nan_bytes_match_torch():
+    """Reading R1: a NaN becomes S.1111111 with its sign, the bytes torch's
+    float8 casts produce for both signs; a NaN product (an infinity times a
+    zero multiplier) takes the input element's sign."""
     import torch
 
     x = np.array([np.nan, -np.nan], np.float32)
     for fmt, dt in ((O.E4M3, torch.float8_e4m3fn), (O.E5M2, torch.float8_e5m2)):
         lib = torch.from_numpy(x).to(dt).view(torch.uint8).numpy()
-        got = O.convert(x, O.F32, fmt)
-        assert got[0] == lib[0] == 0x7F
-        assert got[1] == 0x7F and lib[1] == 0xFF
+        np.testing.assert_array_equal(O.convert(x, O.F32, fmt), lib)
+        np.testing.assert_array_equal(lib, [0x7F, 0xFF])
+        np.testing.assert_array_equal(O.fp8_cast_array(np.array([np.inf, -np.inf], np.float32), O.F32, fmt, 0.0),
+                                      [0x7F, 0xFF])
 
 
 @pytest.mark.parametrize("fmt,fmax", [(O.E4M3, 448.0), (O.E5M2, 57344.0)])
