@@ -63,7 +63,7 @@ uint16_t orc_f32_to_f16(float x) {
 float orc_f16_to_f32(uint16_t h) {
   uint32_t e = (h >> 10) & 0x1F, m = h & 0x3FF;
   float sgn = (h & 0x8000) ? -1.0f : 1.0f;
-  if (e == 31) return m ? NAN : sgn * INFINITY;
+  if (e == 31) return m ? copysignf(NAN, sgn) : sgn * INFINITY; /* a NaN keeps its sign */
   return sgn * (float)decode_mag(e, m, 10, -14, 15);
 }
 
@@ -82,7 +82,7 @@ uint16_t orc_f32_to_bf16(float x) {
 float orc_bf16_to_f32(uint16_t h) {
   uint32_t e = (h >> 7) & 0xFF, m = h & 0x7F;
   float sgn = (h & 0x8000) ? -1.0f : 1.0f;
-  if (e == 255) return m ? NAN : sgn * INFINITY;
+  if (e == 255) return m ? copysignf(NAN, sgn) : sgn * INFINITY; /* a NaN keeps its sign */
   return sgn * (float)decode_mag(e, m, 7, -126, 127);
 }
 
@@ -118,9 +118,9 @@ float orc_fp8_to_f32(uint8_t c, int fmt) {
   uint32_t e = (c & 0x7F) >> M, m = c & ((1u << M) - 1);
   float sgn = (c & 0x80) ? -1.0f : 1.0f;
   if (fmt == ORC_E4M3) {
-    if (e == 15 && m == 7) return NAN;
+    if (e == 15 && m == 7) return copysignf(NAN, sgn);
   } else if (e == 31) {
-    return m ? NAN : sgn * INFINITY;
+    return m ? copysignf(NAN, sgn) : sgn * INFINITY;
   }
   return sgn * (float)decode_mag(e, m, M, emin, bias);
 }

@@ -148,6 +148,12 @@ def test_nan_bytes_match_torch():
         np.testing.assert_array_equal(lib, [0x7F, 0xFF])
         np.testing.assert_array_equal(O.fp8_cast_array(np.array([np.inf, -np.inf], np.float32), O.F32, fmt, 0.0),
                                       [0x7F, 0xFF])
+        # 16-bit NaN inputs of both signs (every NaN payload) keep their sign too
+        for src, tdt, fmt16 in ((np.arange(0x7F81, 0x7FFF + 1), torch.bfloat16, O.BF16),
+                                (np.arange(0x7C01, 0x7FFF + 1), torch.float16, O.F16)):
+            bits = np.concatenate([src, src | 0x8000]).astype(np.uint16)
+            want = torch.from_numpy(bits.view(np.int16)).view(tdt).to(dt).view(torch.uint8).numpy()
+            np.testing.assert_array_equal(O.fp8_cast_array(bits, fmt16, fmt, 1.0), want)
 
 
 @pytest.mark.parametrize("fmt,fmax", [(O.E4M3, 448.0), (O.E5M2, 57344.0)])
