@@ -126,10 +126,16 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
   }
 }
 
+// FP8 byte of a NaN product: S.1111111 with the sign of input element a.
+__device__ __forceinline__ uint8_t nan_byte(float a) {
+  return (uint8_t)(0x7Fu | ((__float_as_uint(a) >> 24) & 0x80u));
+}
+
 // Casts one raw 16-element vector with multiplier `scale`; returns the 16
 // output bytes and the vector's NaN-propagating max |x| in *vmax.  A NaN
 // product (a NaN input, or an infinite input times a zero multiplier) gives
-// 0x7F; the products are checked, not the inputs.
+// 0x7F with the input element's sign bit (0xFF when negative); the products
+// are checked, the sign is read from the input.
 template <int XT, bool E5M2>
 __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out,
                                         uint32_t* saturated = nullptr) {
@@ -153,8 +159,8 @@ __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, floa
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float2 f = pair_of<XT>(raw, k);
-      if (__fmul_rn(f.x, scale) != __fmul_rn(f.x, scale)) ob[2 * k] = 0x7F;
-      if (__fmul_rn(f.y, scale) != __fmul_rn(f.y, scale)) ob[2 * k + 1] = 0x7F;
+      if (__fmul_rn(f.x, scale) != __fmul_rn(f.x, scale)) ob[2 * k] = nan_byte(f.x);
+      if (__fmul_rn(f.y, scale) != __fmul_rn(f.y, scale)) ob[2 * k + 1] = nan_byte(f.y);
     }
   }
   *vmax_out = vmax;
@@ -201,7 +207,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
       acc = max_abs_nan(acc, a);
       const float p = __fmul_rn(a, scale);
       uint32_t b = cast_pair<E5M2>(p, 0.0f) & 0xFFu;
-      if (p != p) b = 0x7F;
+      if (p != p) b = nan_byte(a);
       y[i] = (uint8_t)b;
       if (COUNT) sat += fabsf(p) > (E5M2 ? 57344.0f : 448.0f);
     }
