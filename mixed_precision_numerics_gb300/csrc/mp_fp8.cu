@@ -55,6 +55,27 @@ __device__ __forceinline__ float2 pair_of(const uint4 (&r)[4], int k) {
   }
 }
 
+// Sign bits of element pair k of a raw vector, as 0x80 or 0 per element.  Read
+// from the stored bits: the FP16 -> FP32 conversion does not keep a NaN's sign.
+template <int XT>
+__device__ __forceinline__ uint2 signs_of(const uint4 (&r)[4], int k) {
+  if constexpr (XT == XF32) {
+    const uint4 q = r[k >> 1];
+    const uint32_t a = (k & 1) ? q.z : q.x, b = (k & 1) ? q.w : q.y;
+    return make_uint2((a >> 24) & 0x80u, (b >> 24) & 0x80u);
+  } else {
+    const uint4 q = r[k >> 2];
+    const uint32_t w = (k & 3) == 0 ? q.x : (k & 3) == 1 ? q.y : (k & 3) == 2 ? q.z : q.w;
+    return make_uint2((w >> 8) & 0x80u, (w >> 24) & 0x80u);
+  }
+}
+
+template <int XT>
+__device__ __forceinline__ uint32_t sign1(const void* x, int64_t i) {
+  if constexpr (XT == XF32) return (static_cast<const uint32_t*>(x)[i] >> 24) & 0x80u;
+  return (static_cast<const uint16_t*>(x)[i] >> 8) & 0x80u;
+}
+
 template <int XT>
 __device__ __forceinline__ float load1(const void* x, int64_t i) {
   if constexpr (XT == XF32) return static_cast<const float*>(x)[i];
@@ -126,10 +147,8 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
   }
 }
 
-// FP8 byte of a NaN product: S.1111111 with the sign of input element a.
-__device__ __forceinline__ uint8_t nan_byte(float a) {
-  return (uint8_t)(0x7Fu | ((__float_as_uint(a) >> 24) & 0x80u));
-}
+// FP8 byte of a NaN product: S.1111111 with the input element's sign bit.
+__device__ __forceinline__ uint8_t nan_byte(uint32_t sign80) { return (uint8_t)(0x7Fu | sign80); }
 
 // Casts one raw 16-element vector with multiplier `scale`; returns the 16
 // output bytes and the vector's NaN-propagating max |x| in *vmax.  A NaN
@@ -159,8 +178,9 @@ __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, floa
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
       const float2 f = pair_of<XT>(raw, k);
-      if (__fmul_rn(f.x, scale) != __fmul_rn(f.x, scale)) ob[2 * k] = nan_byte(f.x);
-      if (__fmul_rn(f.y, scale) != __fmul_rn(f.y, scale)) ob[2 * k + 1] = nan_byte(f.y);
+      const uint2 sg = signs_of<XT>(raw, k);
+      if (__fmul_rn(f.x, scale) != __fmul_rn(f.x, scale)) ob[2 * k] = nan_byte(sg.x);
+      if (__fmul_rn(f.y, scale) != __fmul_rn(f.y, scale)) ob[2 * k + 1] = nan_byte(sg.y);
     }
   }
   *vmax_out = vmax;
@@ -207,7 +227,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
       acc = max_abs_nan(acc, a);
       const float p = __fmul_rn(a, scale);
       uint32_t b = cast_pair<E5M2>(p, 0.0f) & 0xFFu;
-      if (p != p) b = nan_byte(a);
+      if (p != p) b = nan_byte(sign1<XT>(x, i));
       y[i] = (uint8_t)b;
       if (COUNT) sat += fabsf(p) > (E5M2 ? 57344.0f : 448.0f);
     }
