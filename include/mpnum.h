@@ -65,6 +65,13 @@ MP_API const char* mp_status_str(mp_status s);
 MP_API int32_t mp_version(void);
 /* Number of kernels this library has launched in this process (diagnostic). */
 MP_API uint64_t mp_launch_count(void);
+/* Number of bounded waits on a tile copy that gave up inside this library's
+ * FP8 kernels since it was loaded (0 in normal operation).  A kernel whose
+ * copy engine stopped answering waits about two seconds per wait, counts the
+ * failure here and returns; the outputs of that call are then incomplete.
+ * Reads device memory synchronously: call it after synchronising the streams
+ * that ran the calls.  *out written; MP_EINVAL if out is NULL. */
+MP_API mp_status mp_wait_failures(uint32_t* out);
 
 /* =========================================================================
  * 1. Mixed-precision optimizer step
@@ -261,7 +268,10 @@ MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int
  * y = saturate(RNE(fp32(x) * r)) with r = fp8_max / amax if amax is finite
  * and > 0, else r = 0 (a NaN product gives 0x7F or, for a negative input
  * element, 0xFF).  Each block is read once.
- * cols % 16 == 0; x, y 16-byte aligned.  One kernel launch. */
+ * cols % 16 == 0 (and rows, cols < 2^31 for 128x128 blocks, else
+ * MP_ESHAPE); x, y 16-byte aligned.  One kernel launch.  The 128x128 form
+ * reads its blocks through 2-D tensor copies; it returns MP_ECUDA if the
+ * driver's tensor-map encoder is unavailable. */
 MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
                                         int32_t block_rows, int32_t block_cols, void* y, mp_dtype fp8_dtype,
                                         float* scales, void* stream);

@@ -93,6 +93,7 @@ def _load() -> ctypes.CDLL:
         "mp_status_str": (ctypes.c_char_p, [I32]),
         "mp_version": (I32, []),
         "mp_launch_count": (U64, []),
+        "mp_wait_failures": (I32, [P]),
         "mp_scaler_state_init": (None, [P, F]),
         "mp_fp8_meta_init": (None, [P]),
         "mp_adamw_workspace_size": (S, [P, I32]),
@@ -162,6 +163,13 @@ def mp_status_str(status: int) -> str:
 
 def mp_launch_count() -> int:
     return int(lib.mp_launch_count())
+
+
+def mp_wait_failures() -> int:
+    """Bounded tile-copy waits that gave up in the library's FP8 kernels (0 normally)."""
+    out = ctypes.c_uint32(0)
+    _check("mp_wait_failures", lib.mp_wait_failures(ctypes.byref(out)))
+    return int(out.value)
 
 
 def nvfp4_workspace_size() -> int:
@@ -370,7 +378,7 @@ __all__ = [
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
     "fp8_cast_transpose_delayed", "fp8_cast_delayed_count", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
     "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
-    "nvfp4_workspace_size", "mp_status_str", "mp_launch_count",
+    "nvfp4_workspace_size", "mp_status_str", "mp_launch_count", "mp_wait_failures",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",
     "make_param_array",
 ]

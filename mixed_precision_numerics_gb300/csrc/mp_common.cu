@@ -1,4 +1,6 @@
 // mp_common.cu — status strings, version, launch counter, state initialisers.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <string.h>
 
@@ -23,6 +25,38 @@ int sm_count() {
   return n;
 }
 
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link against the driver library).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 f = fn.load(std::memory_order_acquire);
+  if (f) return f;
+  void* p = nullptr;
+  cudaDriverEntryPointQueryResult q{};
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !p)
+    return nullptr;
+  f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  fn.store(f, std::memory_order_release);
+  return f;
+}
+
+bool encode_tile_map_2d(CUtensorMap* map, const void* base, int esize, int64_t rows, int64_t cols, int box_rows,
+                        int box_cols) {
+  if (rows < 1 || cols < 1 || rows >= (1ll << 31) || cols >= (1ll << 31)) return false;  // int32 box coordinates
+  if ((reinterpret_cast<uintptr_t>(base) & 15u) || ((cols * esize) & 15)) return false;
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const CUtensorMapDataType dt = esize == 4 ? CU_TENSOR_MAP_DATA_TYPE_UINT32 : CU_TENSOR_MAP_DATA_TYPE_UINT16;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t pitch[1] = {(cuuint64_t)(cols * esize)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t unit[2] = {1, 1};
+  return enc(map, dt, 2, const_cast<void*>(base), dims, pitch, box, unit, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace mp
 
 extern "C" {
@@ -40,6 +74,12 @@ MP_API const char* mp_status_str(mp_status s) {
 }
 
 MP_API int32_t mp_version(void) { return 10000; }
+
+MP_API mp_status mp_wait_failures(uint32_t* out) {
+  if (!out) return MP_EINVAL;
+  *out = mp::fp8_wait_failures();
+  return MP_OK;
+}
 
 MP_API uint64_t mp_launch_count(void) { return mp::g_launches.load(std::memory_order_relaxed); }
 

@@ -101,6 +101,19 @@ __device__ __forceinline__ float max_abs_nan(float acc, float a) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(acc), "f"(fabsf(a)));
   return r;
 }
+// NaN-propagating max of the magnitudes of a packed 16-bit pair w into the
+// packed magnitudes acc (PTX max.NaN on bf16x2 / f16x2; a NaN lane becomes the
+// canonical NaN of its half).
+template <bool BF16>
+__device__ __forceinline__ uint32_t max_abs_nan_x2(uint32_t acc, uint32_t w) {
+  uint32_t r;
+  const uint32_t a = w & 0x7FFF7FFFu;
+  if constexpr (BF16)
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(a));
+  else
+    asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(acc), "r"(a));
+  return r;
+}
 // Non-negative float or NaN -> ordered bits, NaN canonical (0x7FC00000).
 __device__ __forceinline__ uint32_t amax_bits(float a) {
   return (a != a) ? 0x7FC00000u : __float_as_uint(a);
@@ -254,6 +267,25 @@ __device__ __forceinline__ uint4 ld_hint(const void* p, uint64_t policy) {
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p), "l"(policy));
   return r;
+}
+// 2-D tiled tensor copy (TMA) of the box at element coordinates (x, y), x the
+// innermost, into dst, completing its bytes on `bar`.  The map lives in
+// kernel-parameter space (__grid_constant__).  x * element size must be a
+// multiple of 16 bytes; parts of the box outside the tensor read as zero.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int32_t x, int32_t y, uint64_t* bar,
+                                           uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_tensor_map(const void* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+// Barrier `id` (1..15) over `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -437,6 +437,250 @@ __global__ __launch_bounds__(kThreads) void k_fp8_block_128x128(const void* __re
   }
 }
 
+// ---------------------------------------------------------------------------
+// 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
+// a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
+// shared-memory stages (kRingBytes: six 32 KB stages for 16-bit input, three
+// 64 KB for FP32).  The consumers are kGroups groups of eight warps; group g
+// takes the CTA's rounds g, g + kGroups, ..., so several blocks are reduced
+// and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
+// elements) of the stage into registers and releases the stage at once, so
+// the next copy starts while the block is reduced (four independent maxima,
+// warp shuffles, then one named barrier per group, the partial maxima
+// double-buffered by round) and cast from registers.  Warp w of a group takes
+// rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15), whole rows,
+// so shared-memory reads cover 512 consecutive bytes per instruction and
+// every store writes whole row segments.  Parts of an edge block outside the
+// tensor arrive as zeros, which leave the amax unchanged, and are not stored.
+// ---------------------------------------------------------------------------
+constexpr int kGroupWarps = 8;
+constexpr int kGroupThreads = 32 * kGroupWarps;
+constexpr int kRingBytes = 192 * 1024;
+
+__device__ unsigned int g_wait_failures;  // bounded waits that gave up (read by mp_wait_failures)
+
+template <int XT>
+struct BlkGeom {
+  static constexpr int kEs = XT == XF32 ? 4 : 2;                 // input element bytes
+  static constexpr int kG = 16 / kEs;                             // elements per 16-byte group
+  static constexpr int kStage = 128 * 128 * kEs;                  // one block
+  static constexpr int kStages = kRingBytes / kStage;             // 6 or 3
+  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 16-byte groups per consumer thread: 8 or 16
+  static constexpr int kGroups = XT == XF32 ? 2 : 3;              // consumer groups (register budget)
+  static constexpr int kThreads = kGroups * kGroupThreads + 32;   // + the producer warp
+  static constexpr size_t kSmem = (size_t)kStages * kStage + 2 * kStages * sizeof(uint64_t) +
+                                  (size_t)kGroups * 2 * kGroupWarps * sizeof(uint32_t);
+};
+
+// One 16-byte group of raw input (8 16-bit or 4 FP32 elements) cast with
+// multiplier r: 8 (or 4) output bytes, element 0 in the lowest byte.  NaN
+// products take S.1111111 with the input element's sign.
+template <int XT, bool E5M2>
+__device__ __forceinline__ uint2 cast_group(const uint4 q, float r) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if constexpr (XT == XF32) {
+    float p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __fmul_rn(__uint_as_float(w[i]), r);
+    uint32_t o = cast_pair<E5M2>(p[0], p[1]) | (cast_pair<E5M2>(p[2], p[3]) << 16);
+    if (__builtin_expect((p[0] != p[0]) | (p[1] != p[1]) | (p[2] != p[2]) | (p[3] != p[3]), 0)) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (p[i] != p[i]) o = (o & ~(0xFFu << (8 * i))) | ((uint32_t)nan_byte((w[i] >> 24) & 0x80u) << (8 * i));
+    }
+    return make_uint2(o, 0u);
+  } else {
+    float p[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = XT == XBF16 ? bf16lo(w[k]) : f16lo(w[k]);
+      const float hi = XT == XBF16 ? bf16hi(w[k]) : f16hi(w[k]);
+      p[2 * k] = __fmul_rn(lo, r);
+      p[2 * k + 1] = __fmul_rn(hi, r);
+    }
+    uint32_t o[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      o[h] = cast_pair<E5M2>(p[4 * h], p[4 * h + 1]) | (cast_pair<E5M2>(p[4 * h + 2], p[4 * h + 3]) << 16);
+    bool any = false;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) any |= p[i] != p[i];
+    if (__builtin_expect(any, 0)) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t sg = (w[i >> 1] >> ((i & 1) ? 24 : 8)) & 0x80u;
+        if (p[i] != p[i]) o[i >> 2] = (o[i >> 2] & ~(0xFFu << (8 * (i & 3)))) | ((uint32_t)nan_byte(sg) << (8 * (i & 3)));
+      }
+    }
+    return make_uint2(o[0], o[1]);
+  }
+}
+
+// NaN-propagating max magnitude of a group, word j into accumulator j: FP32
+// words as floats, 16-bit pairs packed (the two halves are folded at the end).
+template <int XT>
+__device__ __forceinline__ void group_max(const uint4 q, uint32_t (&acc)[4]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    if constexpr (XT == XF32)
+      acc[j] = __float_as_uint(max_abs_nan(__uint_as_float(acc[j]), __uint_as_float(w[j])));
+    else
+      acc[j] = max_abs_nan_x2<XT == XBF16>(acc[j], w[j]);
+  }
+}
+
+// The four accumulators of group_max folded to one float (NaN if any is NaN).
+template <int XT>
+__device__ __forceinline__ float fold_max(const uint32_t (&acc)[4]) {
+  if constexpr (XT == XF32) {
+    return max_abs_nan(max_abs_nan(__uint_as_float(acc[0]), __uint_as_float(acc[1])),
+                       max_abs_nan(__uint_as_float(acc[2]), __uint_as_float(acc[3])));
+  } else {
+    const uint32_t m = max_abs_nan_x2<XT == XBF16>(max_abs_nan_x2<XT == XBF16>(acc[0], acc[1]),
+                                                   max_abs_nan_x2<XT == XBF16>(acc[2], acc[3]));
+    const float lo = XT == XBF16 ? bf16lo(m) : f16lo(m), hi = XT == XBF16 ? bf16hi(m) : f16hi(m);
+    return max_abs_nan(lo, hi);
+  }
+}
+
+// cast_group for a block whose amax is finite: every product is finite and at
+// most fp8_max (1 + 2^-22) in magnitude, which the saturating conversion takes
+// to fp8_max, so neither the clamp nor the NaN repair is needed.
+template <int XT, bool E5M2>
+__device__ __forceinline__ uint2 cast_group_finite(const uint4 q, float r) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t h[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float a, b;
+    if constexpr (XT == XF32) {
+      if (k >= 2) break;
+      a = __uint_as_float(w[2 * k]);
+      b = __uint_as_float(w[2 * k + 1]);
+    } else {
+      a = XT == XBF16 ? bf16lo(w[k]) : f16lo(w[k]);
+      b = XT == XBF16 ? bf16hi(w[k]) : f16hi(w[k]);
+    }
+    const float p0 = __fmul_rn(a, r), p1 = __fmul_rn(b, r);
+    h[k] = E5M2 ? cvt_e5m2x2(p0, p1) : cvt_e4m3x2(p0, p1);
+  }
+  if constexpr (XT == XF32) return make_uint2(h[0] | (h[1] << 16), 0u);
+  return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+}
+
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_128x128_tma(
+    const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
+    float* __restrict__ scales) {
+  using Gm = BlkGeom<XT>;
+  constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG;  // groups per row
+  constexpr int kNG = Gm::kGroups;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kS * kSB);
+  uint64_t* empty = full + kS;
+  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGroupWarps]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nbc = (cols + 127) / 128, nb = ((rows + 127) / 128) * nbc;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kGroupWarps);  // the eight warps of the group that reads the stage
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kNG * kGroupWarps) {
+    // Producer: one lane issues the block copies.
+    if (lane != 0) return;
+    prefetch_tensor_map(&map);
+    const uint64_t policy = policy_evict_first();
+    int issued = 0;
+    bool ok = true;
+    for (int64_t b = blockIdx.x; b < nb; b += gridDim.x, ++issued) {
+      const int sidx = issued % kS;
+      if (!mbar_wait_bounded(&empty[sidx], ((issued / kS) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[sidx], kSB);
+      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128), &full[sidx],
+                  policy);
+    }
+    if (!ok) {
+      atomicAdd(&g_wait_failures, 1u);
+      // Let the copies already issued land before the block's shared memory goes away.
+      for (int k = issued - kS < 0 ? 0 : issued - kS; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % kS], (k / kS) & 1);
+    }
+    return;
+  }
+
+  // Consumers.  A warp whose wait gave up stops reading and storing but keeps
+  // meeting its group's named barrier every round, so the group never blocks on it.
+  const int grp = warp / kGroupWarps, gw = warp % kGroupWarps, t = threadIdx.x % kGroupThreads;
+  constexpr int kRowStep = kGroupThreads / kGpr;  // rows between a thread's groups: 16 or 8
+  uint32_t* gred = red + grp * 2 * kGroupWarps;
+  bool ok = true;
+  int it = grp, round = 0;
+  for (int64_t b = blockIdx.x + (int64_t)grp * gridDim.x; b < nb; b += (int64_t)kNG * gridDim.x, it += kNG, ++round) {
+    const int sidx = it % kS;
+    if (ok) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[sidx], (it / kS) & 1));
+      if (!ok && lane == 0) atomicAdd(&g_wait_failures, 1u);
+    }
+    uint4 raw[Gm::kGpt];
+    uint32_t acc[4] = {0u, 0u, 0u, 0u};
+    if (ok) {
+      const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) group_max<XT>(raw[k], acc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sidx]);  // the stage's bytes are all in registers
+    }
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits(fold_max<XT>(acc)));
+    if (lane == 0) gred[(round & 1) * kGroupWarps + gw] = m;
+    named_barrier(1 + grp, kGroupThreads);
+    if (!ok) continue;
+    uint32_t mb = 0;
+#pragma unroll
+    for (int w = 0; w < kGroupWarps; ++w) mb = max(mb, gred[(round & 1) * kGroupWarps + w]);
+    const float amax = __uint_as_float(mb);
+    float sc, r;
+    block_scale_of<E5M2>(amax, &sc, &r);
+    const int64_t row0 = (b / nbc) * 128 + t / kGpr, col = (b % nbc) * 128 + (t % kGpr) * kG;
+    uint8_t* yp = y + row0 * cols + col;
+    const int64_t rows_left = rows - row0;  // this thread's rows k * kRowStep < rows_left exist
+    if (col < cols) {
+      if (isfinite(amax)) {
+#pragma unroll
+        for (int k = 0; k < Gm::kGpt; ++k) {
+          if (k * kRowStep >= rows_left) break;
+          const uint2 o = cast_group_finite<XT, E5M2>(raw[k], r);
+          if constexpr (XT == XF32)
+            __stcs(reinterpret_cast<uint32_t*>(yp + (int64_t)k * kRowStep * cols), o.x);
+          else
+            __stcs(reinterpret_cast<uint2*>(yp + (int64_t)k * kRowStep * cols), o);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < Gm::kGpt; ++k) {
+          if (k * kRowStep >= rows_left) break;
+          const uint2 o = cast_group<XT, E5M2>(raw[k], r);
+          if constexpr (XT == XF32)
+            __stcs(reinterpret_cast<uint32_t*>(yp + (int64_t)k * kRowStep * cols), o.x);
+          else
+            __stcs(reinterpret_cast<uint2*>(yp + (int64_t)k * kRowStep * cols), o);
+        }
+      }
+    }
+    if (t == 0) scales[b] = sc;
+  }
+}
+
 template <typename K>
 int occ_of(K kernel) {
   int o = 0;
@@ -473,9 +717,15 @@ template <int XT, bool E5M2>
 mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool square, uint8_t* y, float* scales,
                            cudaStream_t s) {
   if (square) {
-    static const int occ = occ_of(k_fp8_block_128x128<XT, E5M2>);
+    using Gm = BlkGeom<XT>;
+    CUtensorMap map;
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_fp8_block_128x128_tma<XT, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
+    if (attr != cudaSuccess) return MP_ECUDA;
     const int64_t blocks = ((rows + 127) / 128) * ((cols + 127) / 128);
-    k_fp8_block_128x128<XT, E5M2><<<grid_for(blocks, occ), kThreads, 0, s>>>(x, rows, cols, y, scales);
+    k_fp8_block_128x128_tma<XT, E5M2><<<grid_for(blocks, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y,
+                                                                                            scales);
   } else {
     static const int occ = occ_of(k_fp8_block_1x128<XT, E5M2>);
     const int64_t quads = (rows * ((cols + 127) / 128) + 3) / 4;
@@ -524,6 +774,13 @@ mp_status cast_entry(const void* x, mp_dtype x_dtype, int64_t n, void* y, mp_dty
 }
 
 }  // namespace
+
+uint32_t fp8_wait_failures() {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_wait_failures, sizeof(v)) != cudaSuccess) return 0xFFFFFFFFu;
+  return v;
+}
+
 }  // namespace mp
 
 extern "C" MP_API mp_status fp8_cast_delayed(const void* x, mp_dtype x_dtype, int64_t n, void* y,
@@ -583,6 +840,7 @@ extern "C" MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dty
   const bool square = block_rows == 128 && block_cols == 128;
   if (!square && !(block_rows == 1 && block_cols == 128)) return MP_ESHAPE;
   if (cols % 16 != 0) return MP_ESHAPE;
+  if (square && (rows >= (1ll << 31) || cols >= (1ll << 31))) return MP_ESHAPE;  // 32-bit tile coordinates
   if (n > 0 && (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(scales) & 3u))) return MP_EALIGN;
   if (n == 0) return MP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -1,6 +1,7 @@
 // mp_internal.h — host-side helpers shared by the libmpnum translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (types only; the encoder is reached through the runtime)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,17 @@ inline int grid_for(int64_t work_ctas, int per_sm) {
   if (work_ctas < 1) work_ctas = 1;
   return (int)(work_ctas < cap ? work_ctas : cap);
 }
+
+// Encodes a 2-D row-major tensor [rows, cols] of `esize`-byte elements at
+// `base` as a TMA tile map with box [box_rows, box_cols], no swizzle, zero
+// fill outside the tensor.  False if the driver's encoder is unavailable or
+// refuses the layout (base not 16-byte aligned, row pitch not a multiple of 16
+// bytes, an extent of 2^31 or more: box coordinates are 32-bit signed).
+bool encode_tile_map_2d(CUtensorMap* map, const void* base, int esize, int64_t rows, int64_t cols, int box_rows,
+                        int box_cols);
+
+// Bounded waits that gave up in this library's kernels since it was loaded.
+uint32_t fp8_wait_failures();
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

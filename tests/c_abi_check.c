@@ -40,6 +40,7 @@ int main(void) {
                        (void*)16, 256, NULL) == MP_ESHAPE);
   CHECK(mx_quantize((void*)16, MP_BF16, 2, 48, MP_E2M1, (void*)16, (uint8_t*)16, NULL, NULL) == MP_ESHAPE);
   CHECK(rht16((void*)16, 2, 40, 0, (void*)16, MP_F32, NULL) == MP_ESHAPE);
+  CHECK(mp_wait_failures(NULL) == MP_EINVAL);
   CHECK(mp_launch_count() == 0);
   printf("c abi ok\n");
   return 0;

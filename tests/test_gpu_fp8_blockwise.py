@@ -99,3 +99,21 @@ def test_empty_tensor_launches_nothing():
         M.fp8_quantize_blockwise(x, torch.empty(0, dtype=torch.uint8, device="cuda"),
                                  torch.empty(0, device="cuda"), br, 128)
     assert M.mp_launch_count() == n0
+
+
+@pytest.mark.parametrize("shape,dtype", [((4000, 7184), torch.bfloat16), ((3000, 4112), torch.float32),
+                                         ((2049, 6160), torch.float16)])
+def test_many_blocks_per_cta_ragged(shape, dtype):
+    """Enough 128x128 blocks that every CTA's ring of tile copies wraps several
+    times, with partial blocks on the right and bottom edges."""
+    x, xt = make_input(*shape, dtype, 3)
+    for fmt, ofmt in ((M.MP_E4M3, O.E4M3), (M.MP_E5M2, O.E5M2)):
+        y, sc = gpu_blockwise(xt, 128, 128, fmt)
+        ry, rsc = O.fp8_quantize_blockwise(x, XFMT[dtype], 128, 128, ofmt)
+        np.testing.assert_array_equal(sc.view(np.uint32), rsc.view(np.uint32))
+        assert np.array_equal(y, ry)
+    assert M.mp_wait_failures() == 0
+
+
+def test_no_wait_gave_up():
+    assert M.mp_wait_failures() == 0
