@@ -333,110 +333,6 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
   *r = (isfinite(amax) && amax > 0.0f) ? __fdiv_rn(fmax, amax) : 0.0f;
 }
 
-// Quads per warp iteration.  Deeper unrolls (2 or 4 quads, 64-128 B in flight
-// per thread) measured slower on the [8192 x 4096] activations: their register
-// use cuts the resident CTAs per SM more than the extra loads in flight help.
-template <int XT>
-__host__ __device__ constexpr int quads_of() { return 1; }
-
-// 1 x 128 tiles: eight threads per tile (16 elements each), four tiles per
-// warp ("a quad"); each warp takes U quads per iteration with all their loads
-// issued first.  Quad validity is uniform across the warp, so every lane takes
-// part in the width-8 shuffles.
-template <int XT, bool E5M2>
-__global__ __launch_bounds__(kThreads) void k_fp8_block_1x128(const void* __restrict__ x, int64_t rows,
-                                                              int64_t cols, uint8_t* __restrict__ y,
-                                                              float* __restrict__ scales) {
-  constexpr int U = quads_of<XT>();
-  constexpr int kWarps = kThreads / 32;
-  const int64_t ntc = (cols + 127) / 128;
-  const int64_t ntiles = rows * ntc;
-  const int64_t nquads = (ntiles + 3) / 4;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 3, l8 = lane & 7;
-  for (int64_t q0 = (int64_t)blockIdx.x * kWarps * U + warp; q0 < nquads; q0 += (int64_t)gridDim.x * kWarps * U) {
-    uint4 raw[U][4];
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t tile = (q0 + (int64_t)u * kWarps) * 4 + g;
-      const int64_t row = tile / ntc, col = (tile % ntc) * 128 + l8 * 16;
-      if (tile < ntiles && col < cols) load_raw<XT>(x, (row * cols + col) / kElems, raw[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t q = q0 + (int64_t)u * kWarps;
-      if (q >= nquads) break;  // warp-uniform
-      const int64_t tile = q * 4 + g;
-      const int64_t row = tile / ntc, tc = tile % ntc;
-      const int64_t col = tc * 128 + l8 * 16;
-      const bool valid = tile < ntiles && col < cols;
-      float vmax = 0.0f;
-      if (valid) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 f = pair_of<XT>(raw[u], k);
-          vmax = max_abs_nan(vmax, f.x);
-          vmax = max_abs_nan(vmax, f.y);
-        }
-      }
-#pragma unroll
-      for (int h = 4; h >= 1; h >>= 1) {
-        const float o = __shfl_xor_sync(0xFFFFFFFFu, vmax, h, 8);
-        vmax = max_abs_nan(vmax, o);
-      }
-      if (!valid) continue;
-      const float amax = vmax != vmax ? __uint_as_float(0x7FC00000u) : vmax;
-      float s, r, unused;
-      block_scale_of<E5M2>(amax, &s, &r);
-      st_cs(y + row * cols + col, cast16<XT, E5M2>(raw[u], r, &unused));
-      if (l8 == 0) scales[row * ntc + tc] = s;
-    }
-  }
-}
-
-// 128 x 128 blocks: one CTA per block; thread t owns column segment t % 8 of
-// rows t / 8 + 32 k, k = 0..3, held in registers between the block amax and
-// the cast.
-template <int XT, bool E5M2>
-__global__ __launch_bounds__(kThreads) void k_fp8_block_128x128(const void* __restrict__ x, int64_t rows,
-                                                                int64_t cols, uint8_t* __restrict__ y,
-                                                                float* __restrict__ scales) {
-  __shared__ uint32_t red[32];
-  __shared__ uint32_t amax_b;
-  const int64_t nbr = (rows + 127) / 128, nbc = (cols + 127) / 128;
-  const int cs = threadIdx.x & 7, rr = threadIdx.x >> 3;
-  for (int64_t b = blockIdx.x; b < nbr * nbc; b += gridDim.x) {
-    const int64_t br = b / nbc, bc = b % nbc;
-    const int64_t col = bc * 128 + cs * 16;
-    uint4 raw[4][4];
-    float vmax = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t row = br * 128 + rr + 32 * k;
-      if (row < rows && col < cols) {
-        load_raw<XT>(x, (row * cols + col) / kElems, raw[k]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float2 f = pair_of<XT>(raw[k], j);
-          vmax = max_abs_nan(vmax, f.x);
-          vmax = max_abs_nan(vmax, f.y);
-        }
-      }
-    }
-    const uint32_t m = block_max_u32(amax_bits(vmax), red);
-    if (threadIdx.x == 0) amax_b = m;
-    __syncthreads();
-    float s, r, unused;
-    block_scale_of<E5M2>(__uint_as_float(amax_b), &s, &r);
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t row = br * 128 + rr + 32 * k;
-      if (row < rows && col < cols) st_cs(y + row * cols + col, cast16<XT, E5M2>(raw[k], r, &unused));
-    }
-    if (threadIdx.x == 0) scales[br * nbc + bc] = s;
-    __syncthreads();  // red and amax_b are reused by the next block
-  }
-}
-
 // ---------------------------------------------------------------------------
 // 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
 // a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
@@ -569,8 +465,31 @@ __device__ __forceinline__ uint2 cast_group_finite(const uint4 q, float r) {
   return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-template <int XT, bool E5M2>
-__global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_128x128_tma(
+// Row maxima of a thread's kGpt groups, one per row slot k, reduced over the
+// L = 2 kGpt lanes that share those rows by recursive halving: at the step
+// with n values left, the lane keeps the upper or lower half (by lane bit n)
+// and takes the max with the half its partner at distance n sent, so after
+// log2(kGpt) steps it holds slot ((lane & (2 kGpt - 2)) >> 1), and a last
+// exchange at distance 1 completes it: 2 kGpt - 1 shuffles in all, instead of
+// kGpt log2(L).
+template <int V>
+__device__ __forceinline__ uint32_t row_max_scatter(uint32_t (&v)[V], int lane) {
+#pragma unroll
+  for (int n = V; n >= 2; n >>= 1) {
+    const bool up = (lane & n) != 0;
+#pragma unroll
+    for (int j = 0; j < n / 2; ++j) {
+      const uint32_t keep = up ? v[j + n / 2] : v[j], send = up ? v[j] : v[j + n / 2];
+      v[j] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, n));
+    }
+  }
+  return max(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
+}
+
+// ROWS = false: one scale per 128 x 128 box (block).  ROWS = true: the box is
+// 128 stacked 1 x 128 tiles, one scale per row of it.
+template <int XT, bool E5M2, bool ROWS>
+__global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
     float* __restrict__ scales) {
   using Gm = BlkGeom<XT>;
@@ -631,6 +550,42 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_128x128_
       if (!ok && lane == 0) atomicAdd(&g_wait_failures, 1u);
     }
     uint4 raw[Gm::kGpt];
+    if constexpr (ROWS) {
+      if (!ok) break;  // no barrier to keep meeting: the warp leaves
+      const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
+      uint32_t v[Gm::kGpt];
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) {
+        uint32_t acc[4] = {0u, 0u, 0u, 0u};
+        group_max<XT>(raw[k], acc);
+        v[k] = amax_bits(fold_max<XT>(acc));
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sidx]);  // the stage's bytes are all in registers
+      // This lane's row slot, its amax, scale and multiplier; then every
+      // slot's multiplier from the even lane that holds it.
+      const int slot = (lane & (2 * Gm::kGpt - 2)) >> 1, base = lane & ~(kGpr - 1);
+      const float amax = __uint_as_float(row_max_scatter<Gm::kGpt>(v, lane));
+      float sc, rm;
+      block_scale_of<E5M2>(amax, &sc, &rm);
+      const int64_t bc = b % nbc, row0 = (b / nbc) * 128 + t / kGpr, col = bc * 128 + (t % kGpr) * kG;
+      const int64_t rows_left = rows - row0;
+      if ((lane & 1) == 0 && (int64_t)slot * kRowStep < rows_left) scales[(row0 + slot * kRowStep) * nbc + bc] = sc;
+      uint8_t* yp = y + row0 * cols + col;
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) {
+        const float r = __shfl_sync(0xFFFFFFFFu, rm, base | (k << 1));
+        if (col >= cols || k * kRowStep >= rows_left) continue;
+        const uint2 o = r > 0.0f ? cast_group_finite<XT, E5M2>(raw[k], r) : cast_group<XT, E5M2>(raw[k], r);
+        if constexpr (XT == XF32)
+          __stcs(reinterpret_cast<uint32_t*>(yp + (int64_t)k * kRowStep * cols), o.x);
+        else
+          __stcs(reinterpret_cast<uint2*>(yp + (int64_t)k * kRowStep * cols), o);
+      }
+      continue;
+    }
     uint32_t acc[4] = {0u, 0u, 0u, 0u};
     if (ok) {
       const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
@@ -716,22 +671,20 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
 template <int XT, bool E5M2>
 mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool square, uint8_t* y, float* scales,
                            cudaStream_t s) {
+  using Gm = BlkGeom<XT>;
+  CUtensorMap map;
+  if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
+  const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
   if (square) {
-    using Gm = BlkGeom<XT>;
-    CUtensorMap map;
-    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
     static const cudaError_t attr = cudaFuncSetAttribute(
-        k_fp8_block_128x128_tma<XT, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
+        k_fp8_block_tma<XT, E5M2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
     if (attr != cudaSuccess) return MP_ECUDA;
-    const int64_t blocks = ((rows + 127) / 128) * ((cols + 127) / 128);
-    k_fp8_block_128x128_tma<XT, E5M2><<<grid_for(blocks, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y,
-                                                                                            scales);
+    k_fp8_block_tma<XT, E5M2, false><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
   } else {
-    static const int occ = occ_of(k_fp8_block_1x128<XT, E5M2>);
-    const int64_t quads = (rows * ((cols + 127) / 128) + 3) / 4;
-    const int64_t per_cta = (int64_t)(kThreads / 32) * quads_of<XT>();
-    const int64_t ctas = (quads + per_cta - 1) / per_cta;
-    k_fp8_block_1x128<XT, E5M2><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, rows, cols, y, scales);
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        k_fp8_block_tma<XT, E5M2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
+    if (attr != cudaSuccess) return MP_ECUDA;
+    k_fp8_block_tma<XT, E5M2, true><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
   }
   note_launches(1);
   return launch_status();
@@ -840,7 +793,7 @@ extern "C" MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dty
   const bool square = block_rows == 128 && block_cols == 128;
   if (!square && !(block_rows == 1 && block_cols == 128)) return MP_ESHAPE;
   if (cols % 16 != 0) return MP_ESHAPE;
-  if (square && (rows >= (1ll << 31) || cols >= (1ll << 31))) return MP_ESHAPE;  // 32-bit tile coordinates
+  if (rows >= (1ll << 31) || cols >= (1ll << 31)) return MP_ESHAPE;  // 32-bit tile coordinates
   if (n > 0 && (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(scales) & 3u))) return MP_EALIGN;
   if (n == 0) return MP_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -103,13 +103,14 @@ def test_empty_tensor_launches_nothing():
 
 @pytest.mark.parametrize("shape,dtype", [((4000, 7184), torch.bfloat16), ((3000, 4112), torch.float32),
                                          ((2049, 6160), torch.float16)])
-def test_many_blocks_per_cta_ragged(shape, dtype):
-    """Enough 128x128 blocks that every CTA's ring of tile copies wraps several
-    times, with partial blocks on the right and bottom edges."""
+@pytest.mark.parametrize("block", [(1, 128), (128, 128)])
+def test_many_blocks_per_cta_ragged(shape, dtype, block):
+    """Enough 128 x 128 boxes that every CTA's ring of tile copies wraps several
+    times, with partial boxes (and 1 x 128 tiles) on the right and bottom edges."""
     x, xt = make_input(*shape, dtype, 3)
     for fmt, ofmt in ((M.MP_E4M3, O.E4M3), (M.MP_E5M2, O.E5M2)):
-        y, sc = gpu_blockwise(xt, 128, 128, fmt)
-        ry, rsc = O.fp8_quantize_blockwise(x, XFMT[dtype], 128, 128, ofmt)
+        y, sc = gpu_blockwise(xt, *block, fmt)
+        ry, rsc = O.fp8_quantize_blockwise(x, XFMT[dtype], *block, ofmt)
         np.testing.assert_array_equal(sc.view(np.uint32), rsc.view(np.uint32))
         assert np.array_equal(y, ry)
     assert M.mp_wait_failures() == 0
