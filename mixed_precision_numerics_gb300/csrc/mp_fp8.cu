@@ -12,6 +12,8 @@
 // folds a small slice of the history entries the call does not overwrite into
 // a second word; the last CTA to finish (atomic ticket, no waiting) writes the
 // ring slot and derives the next scale from the two maxima.
+#include <string.h>
+
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -115,17 +117,13 @@ __device__ __forceinline__ void fold_history_slice(mp_fp8_meta* meta, const floa
 // End of every CTA: fold its amax into the meta word; the last CTA (atomic
 // ticket, no waiting) writes the ring slot and derives the next scale from
 // max(history) (algo 0) or from this amax alone (algo 1).
+// The part run by one thread of each CTA, with the CTA's amax bits.
 template <bool E5M2>
-__device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32_t hist_len, int32_t slot,
-                                           float margin, int32_t algo, float acc, uint32_t* red, int* is_last) {
-  const uint32_t cta = block_max_u32(amax_bits(acc), red);
-  if (threadIdx.x == 0) {
-    atomicMax(&meta->internal_amax, cta);
-    __threadfence();
-    *is_last = atomicAdd(&meta->internal_ticket, 1u) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (!*is_last || threadIdx.x != 0) return;
+__device__ __forceinline__ void fp8_finish_one(mp_fp8_meta* meta, float* hist, int32_t hist_len, int32_t slot,
+                                               float margin, int32_t algo, uint32_t cta) {
+  atomicMax(&meta->internal_amax, cta);
+  __threadfence();
+  if (atomicAdd(&meta->internal_ticket, 1u) != gridDim.x - 1) return;
   __threadfence();
   const uint32_t ab = atomicExch(&meta->internal_amax, 0u);
   const uint32_t hm = algo == 1 ? ab : max(atomicExch(&meta->internal_hrest, 0u), ab);
@@ -147,19 +145,39 @@ __device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32
   }
 }
 
+template <bool E5M2>
+__device__ __forceinline__ void fp8_finish(mp_fp8_meta* meta, float* hist, int32_t hist_len, int32_t slot,
+                                           float margin, int32_t algo, float acc, uint32_t* red) {
+  const uint32_t cta = block_max_u32(amax_bits(acc), red);
+  if (threadIdx.x == 0) fp8_finish_one<E5M2>(meta, hist, hist_len, slot, margin, algo, cta);
+}
+
 // FP8 byte of a NaN product: S.1111111 with the input element's sign bit.
 __device__ __forceinline__ uint8_t nan_byte(uint32_t sign80) { return (uint8_t)(0x7Fu | sign80); }
+
+// Saturating RNE conversion of a product pair with no clamp: the conversion's
+// satfinite mode takes every magnitude beyond fp8_max, infinities included,
+// to fp8_max with its sign.  NaN is handled by the caller.
+template <bool E5M2>
+__device__ __forceinline__ uint32_t cvt_pair_sat(float p0, float p1) {
+  return E5M2 ? cvt_e5m2x2(p0, p1) : cvt_e4m3x2(p0, p1);
+}
+
+// True if x * scale can be NaN only where x is NaN.
+__device__ __forceinline__ bool scale_keeps_numbers(float scale) { return scale > 0.0f && scale < INFINITY; }
 
 // Casts one raw 16-element vector with multiplier `scale`; returns the 16
 // output bytes and the vector's NaN-propagating max |x| in *vmax.  A NaN
 // product (a NaN input, or an infinite input times a zero multiplier) gives
-// 0x7F with the input element's sign bit (0xFF when negative); the products
-// are checked, the sign is read from the input.
+// 0x7F with the input element's sign bit (0xFF when negative).  With a
+// finite positive multiplier only a NaN input makes a NaN product, so the
+// vector's own max tells whether the products need checking; otherwise they
+// are checked one by one.  The sign is read from the input.
 template <int XT, bool E5M2>
 __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, float* vmax_out,
                                         uint32_t* saturated = nullptr) {
   constexpr float fmax = E5M2 ? 57344.0f : 448.0f;
-  float vmax = 0.0f, pmax = 0.0f;
+  float vmax = 0.0f;
   uint32_t h[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -167,13 +185,11 @@ __device__ __forceinline__ uint4 cast16(const uint4 (&raw)[4], float scale, floa
     vmax = max_abs_nan(vmax, f.x);
     vmax = max_abs_nan(vmax, f.y);
     const float p0 = __fmul_rn(f.x, scale), p1 = __fmul_rn(f.y, scale);
-    pmax = max_abs_nan(pmax, p0);
-    pmax = max_abs_nan(pmax, p1);
     if (saturated) *saturated += (fabsf(p0) > fmax) + (fabsf(p1) > fmax);  // NaN compares false
-    h[k] = cast_pair<E5M2>(p0, p1);
+    h[k] = cvt_pair_sat<E5M2>(p0, p1);
   }
   uint4 o = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16), h[6] | (h[7] << 16));
-  if (__builtin_expect(pmax != pmax, 0)) {
+  if (__builtin_expect((vmax != vmax) || !scale_keeps_numbers(scale), 0)) {
     uint8_t* ob = reinterpret_cast<uint8_t*>(&o);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -194,7 +210,6 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
                                                        unsigned long long* saturated_out) {
   constexpr int U = unroll_of<XT>();
   __shared__ uint32_t red[32];
-  __shared__ int is_last;
   const float scale = meta->scale;
   const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
   if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
@@ -237,19 +252,8 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
     for (int h = 16; h >= 1; h >>= 1) sat += __shfl_xor_sync(0xFFFFFFFFu, sat, h);
     if ((threadIdx.x & 31) == 0 && sat) atomicAdd(saturated_out, (unsigned long long)sat);
   }
-  fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
+  fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red);
 }
-
-// Cast of a [rows, cols] tensor that also writes the transposed bytes
-// y_t [cols, rows] from the same read.  A CTA takes a 128 x 128 tile: thread
-// t casts the 16-element row segments (t % 8) of rows t / 8 + 32 k, k = 0..3
-// (128 B of input in flight), stores them to y and to a row-major copy of the
-// tile in shared memory.  After one barrier, thread t reads the 32-bit words
-// of column group t % 32 (columns 4 (t % 32) .. + 3) for rows 16 (t / 32) ..
-// + 15 -- each read instruction takes one row's 32 consecutive words, free of
-// bank conflicts -- transposes the 4 x 4 byte blocks with byte permutes and
-// stores four 16-byte row segments of y_t.
-constexpr int kTT = 128;  // tile edge
 
 // 4 x 4 byte transpose: w[i] holds row i (byte j = column j); returns in
 // c[j] the column j (byte i = row i).
@@ -260,64 +264,6 @@ __device__ __forceinline__ void transpose4x4(const uint32_t (&w)[4], uint32_t (&
   c[1] = __byte_perm(a0, a2, 0x7632);
   c[2] = __byte_perm(a1, a3, 0x5410);
   c[3] = __byte_perm(a1, a3, 0x7632);
-}
-
-template <int XT, bool E5M2>
-__global__ __launch_bounds__(kThreads) void k_fp8_cast_t(const void* __restrict__ x, int64_t rows, int64_t cols,
-                                                         uint8_t* __restrict__ y, uint8_t* __restrict__ y_t,
-                                                         mp_fp8_meta* meta, float* hist, int32_t hist_len,
-                                                         float margin, int32_t algo) {
-  constexpr int kRowsPerPass = kThreads / 8;  // 32 rows of 8 segments per pass over the tile
-  __shared__ uint32_t red[32];
-  __shared__ int is_last;
-  __shared__ __align__(16) uint8_t tile[kTT][kTT];
-  const float scale = meta->scale;
-  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;
-  if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
-  const int64_t tiles_r = (rows + kTT - 1) / kTT, tiles_c = (cols + kTT - 1) / kTT;
-  const int lr = threadIdx.x >> 3, seg = (threadIdx.x & 7) * 16;  // row (pass 0) and column segment
-  const int cw = threadIdx.x & 31, rs = (threadIdx.x >> 5) * 16;   // transposed: column group, row run
-  float acc = 0.0f;
-  for (int64_t tt = blockIdx.x; tt < tiles_r * tiles_c; tt += gridDim.x) {
-    const int64_t r0 = (tt / tiles_c) * kTT, c0 = (tt % tiles_c) * kTT;
-    const int64_t col = c0 + seg;
-    uint4 raw[kTT / kRowsPerPass][4];
-#pragma unroll
-    for (int k = 0; k < kTT / kRowsPerPass; ++k) {
-      const int64_t row = r0 + lr + kRowsPerPass * k;
-      if (row < rows && col < cols) load_raw<XT>(x, (row * cols + col) / kElems, raw[k]);
-    }
-#pragma unroll
-    for (int k = 0; k < kTT / kRowsPerPass; ++k) {
-      const int64_t row = r0 + lr + kRowsPerPass * k;
-      if (row < rows && col < cols) {
-        float vmax;
-        const uint4 o = cast16<XT, E5M2>(raw[k], scale, &vmax);
-        acc = max_abs_nan(acc, vmax);
-        st_cs(y + row * cols + col, o);
-        *reinterpret_cast<uint4*>(&tile[lr + kRowsPerPass * k][seg]) = o;
-      }
-    }
-    __syncthreads();
-    const int64_t tcol = c0 + 4 * cw, trow = r0 + rs;
-    if (tcol < cols && trow < rows) {  // cols and rows are multiples of 16: the 4 columns and 16 rows are all in
-      uint32_t out[4][4];  // out[j][m]: column j, rows rs + 4m .. + 3
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        uint32_t w[4], c[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[rs + 4 * m + i][4 * cw]);
-        transpose4x4(w, c);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) out[j][m] = c[j];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        st_cs(y_t + (tcol + j) * rows + trow, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
-    }
-    __syncthreads();  // the tile is rewritten by the next iteration
-  }
-  fp8_finish<E5M2>(meta, hist, hist_len, slot, margin, algo, acc, red, &is_last);
 }
 
 // ---------------------------------------------------------------------------
@@ -440,9 +386,10 @@ __device__ __forceinline__ float fold_max(const uint32_t (&acc)[4]) {
   }
 }
 
-// cast_group for a block whose amax is finite: every product is finite and at
-// most fp8_max (1 + 2^-22) in magnitude, which the saturating conversion takes
-// to fp8_max, so neither the clamp nor the NaN repair is needed.
+// cast_group for products known not to be NaN (a block whose amax is finite,
+// or a NaN-free group under a finite positive scale): the conversion's
+// satfinite mode saturates every larger magnitude, infinities included, so
+// neither the clamp nor the NaN repair is needed.
 template <int XT, bool E5M2>
 __device__ __forceinline__ uint2 cast_group_finite(const uint4 q, float r) {
   const uint32_t w[4] = {q.x, q.y, q.z, q.w};
@@ -459,7 +406,7 @@ __device__ __forceinline__ uint2 cast_group_finite(const uint4 q, float r) {
       b = XT == XBF16 ? bf16hi(w[k]) : f16hi(w[k]);
     }
     const float p0 = __fmul_rn(a, r), p1 = __fmul_rn(b, r);
-    h[k] = E5M2 ? cvt_e5m2x2(p0, p1) : cvt_e4m3x2(p0, p1);
+    h[k] = cvt_pair_sat<E5M2>(p0, p1);
   }
   if constexpr (XT == XF32) return make_uint2(h[0] | (h[1] << 16), 0u);
   return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
@@ -636,6 +583,164 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
   }
 }
 
+// ---------------------------------------------------------------------------
+// Cast + transposed copy through the tensor-copy engine: the same producer and
+// 128 x 128 boxes as above, a 128 KB ring (four 32 KB stages, or two 64 KB for
+// FP32) and kGroups consumer groups on alternate boxes.  A group casts its box
+// from registers with the delayed scale, writes y directly and the same bytes
+// row-major into its own 16 KB shared tile (two per group, alternating by
+// round, so one named barrier per round suffices), then reads the tile back a
+// row of 32 words per instruction, transposes 4 x 4 byte blocks with byte
+// permutes and stores 16-byte row segments of y_t.  The tensor amax is kept
+// per thread and reduced once per CTA at the end.
+// ---------------------------------------------------------------------------
+template <int XT>
+struct TrGeom {
+  static constexpr int kEs = XT == XF32 ? 4 : 2;
+  static constexpr int kG = 16 / kEs;
+  static constexpr int kStage = 128 * 128 * kEs;
+  static constexpr int kStages = (128 * 1024) / kStage;          // 4 or 2
+  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 8 or 16
+  static constexpr int kGroups = XT == XF32 ? 2 : 3;
+  static constexpr int kThreads = kGroups * kGroupThreads + 32;
+  static constexpr int kTile = 128 * 128;                         // cast bytes of one box
+  static constexpr size_t kSmem = (size_t)kStages * kStage + (size_t)kGroups * 2 * kTile +
+                                  2 * kStages * sizeof(uint64_t) + (size_t)kGroups * kGroupWarps * sizeof(uint32_t);
+};
+
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(TrGeom<XT>::kThreads, 1) void k_fp8_cast_t_tma(
+    const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
+    uint8_t* __restrict__ y_t, mp_fp8_meta* meta, float* hist, int32_t hist_len, float margin, int32_t algo) {
+  using Gm = TrGeom<XT>;
+  constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG, kNG = Gm::kGroups;
+  constexpr int kRowStep = kGroupThreads / kGpr;
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* tiles = smem + kS * kSB;  // [kGroups][2][128][128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(tiles + kNG * 2 * Gm::kTile);
+  uint64_t* empty = full + kS;
+  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups * kGroupWarps]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t nbc = (cols + 127) / 128, nb = ((rows + 127) / 128) * nbc;
+  const float scale = meta->scale;
+  const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
+  if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kS; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kGroupWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == kNG * kGroupWarps) {
+    if (lane != 0 || blockIdx.x >= nb) return;
+    prefetch_tensor_map(&map);
+    const uint64_t policy = policy_evict_first();
+    int issued = 0;
+    bool ok = true;
+    for (int64_t b = blockIdx.x; b < nb; b += gridDim.x, ++issued) {
+      const int sidx = issued % kS;
+      if (!mbar_wait_bounded(&empty[sidx], ((issued / kS) & 1) ^ 1)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&full[sidx], kSB);
+      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128), &full[sidx],
+                  policy);
+    }
+    if (!ok) {
+      atomicAdd(&g_wait_failures, 1u);
+      for (int k = issued - kS < 0 ? 0 : issued - kS; k < issued; ++k)
+        (void)mbar_wait_bounded(&full[k % kS], (k / kS) & 1);
+    }
+    return;
+  }
+
+  const int grp = warp / kGroupWarps, t = threadIdx.x % kGroupThreads;
+  const int rs = (t & 7) * 16, cg = t >> 3;  // transposed side: 16-row run, 4-column group
+  const bool scale_ok = scale_keeps_numbers(scale);
+  uint32_t acc = 0u;  // ordered bits of this thread's running max |x|
+  bool ok = true;
+  int it = grp, round = 0;
+  for (int64_t b = blockIdx.x + (int64_t)grp * gridDim.x; b < nb; b += (int64_t)kNG * gridDim.x, it += kNG, ++round) {
+    const int sidx = it % kS;
+    if (ok) {
+      ok = __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[sidx], (it / kS) & 1));
+      if (!ok && lane == 0) atomicAdd(&g_wait_failures, 1u);
+    }
+    const int64_t r0 = (b / nbc) * 128, c0 = (b % nbc) * 128;
+    unsigned char* tile = tiles + (grp * 2 + (round & 1)) * Gm::kTile;
+    if (ok) {
+      uint4 raw[Gm::kGpt];
+      uint32_t racc[4] = {0u, 0u, 0u, 0u};
+      const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) group_max<XT>(raw[k], racc);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[sidx]);
+      const float rmax = fold_max<XT>(racc);
+      acc = max(acc, amax_bits(rmax));
+      const bool clean = scale_ok && rmax == rmax;  // no NaN product possible in this thread's groups
+      const int rin = t / kGpr, cin = (t % kGpr) * kG;
+      const int64_t row0 = r0 + rin, col = c0 + cin;
+      uint8_t* yp = y + row0 * cols + col;
+#pragma unroll
+      for (int k = 0; k < Gm::kGpt; ++k) {
+        const uint2 o = clean ? cast_group_finite<XT, E5M2>(raw[k], scale) : cast_group<XT, E5M2>(raw[k], scale);
+        const int trw = rin + k * kRowStep;
+        unsigned char* tp = tile + trw * 128 + (cin ^ (((trw >> 4) & 7) << 4));  // 16-byte granules XOR-swizzled
+        if constexpr (XT == XF32)
+          *reinterpret_cast<uint32_t*>(tp) = o.x;
+        else
+          *reinterpret_cast<uint2*>(tp) = o;
+        if (col < cols && row0 + k * kRowStep < rows) {
+          if constexpr (XT == XF32)
+            __stcs(reinterpret_cast<uint32_t*>(yp + (int64_t)k * kRowStep * cols), o.x);
+          else
+            __stcs(reinterpret_cast<uint2*>(yp + (int64_t)k * kRowStep * cols), o);
+        }
+      }
+    }
+    named_barrier(1 + grp, kGroupThreads);
+    if (!ok) continue;
+    // Eight consecutive threads cover one column's 128 rows: every store
+    // instruction writes four whole 128-byte lines of y_t.  Rows rs .. rs + 15
+    // share the swizzle (rs / 16), which spreads the eight row runs of a
+    // column group over distinct banks.
+    const int64_t tcol = c0 + 4 * cg, trow = r0 + rs;
+    if (tcol < cols && trow < rows) {  // rows and cols are multiples of 16: the 4 columns and 16 rows are all in
+      const int sw = (4 * cg) ^ ((rs >> 4) << 4);
+      uint32_t out[4][4];  // out[j][m]: column j, rows rs + 4m .. + 3
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        uint32_t w[4], c[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) w[i] = *reinterpret_cast<const uint32_t*>(tile + (rs + 4 * m + i) * 128 + sw);
+        transpose4x4(w, c);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[j][m] = c[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        st_cs(y_t + (tcol + j) * rows + trow, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
+    }
+  }
+  // Tensor amax: warp, then the CTA's consumer warps (one named barrier), then
+  // one thread folds it in and the last CTA finishes the history.
+  const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, acc);
+  if (lane == 0) red[warp] = m;
+  named_barrier(1 + kNG, kNG * kGroupThreads);
+  if (threadIdx.x == 0) {
+    uint32_t cta = 0;
+    for (int w = 0; w < kNG * kGroupWarps; ++w) cta = max(cta, red[w]);
+    fp8_finish_one<E5M2>(meta, hist, hist_len, slot, margin, algo, cta);
+  }
+}
+
 template <typename K>
 int occ_of(K kernel) {
   int o = 0;
@@ -660,10 +765,16 @@ mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float*
 template <int XT, bool E5M2>
 mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_t* y_t, mp_fp8_meta* meta,
                    float* hist, int32_t len, float margin, int32_t algo, cudaStream_t s) {
-  static const int occ = occ_of(k_fp8_cast_t<XT, E5M2>);
-  const int64_t tiles = ((rows + kTT - 1) / kTT) * ((cols + kTT - 1) / kTT);
-  k_fp8_cast_t<XT, E5M2><<<grid_for(tiles, occ), kThreads, 0, s>>>(x, rows, cols, y, y_t, meta, hist, len, margin,
-                                                                    algo);
+  using Gm = TrGeom<XT>;
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));  // an empty tensor still runs one CTA (the history is updated); no copy is issued
+  if (rows > 0 && cols > 0 && !encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
+  static const cudaError_t attr = cudaFuncSetAttribute(
+      k_fp8_cast_t_tma<XT, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
+  if (attr != cudaSuccess) return MP_ECUDA;
+  const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
+  k_fp8_cast_t_tma<XT, E5M2><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, y_t, meta,
+                                                                                 hist, len, margin, algo);
   note_launches(1);
   return launch_status();
 }
@@ -763,6 +874,7 @@ extern "C" MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x
   const mp_status rc = check_common(x_dtype, fp8_dtype, d_meta, d_history, history_len, margin, amax_algo);
   if (rc != MP_OK) return rc;
   if (rows % 16 != 0 || cols % 16 != 0) return MP_ESHAPE;
+  if (rows >= (1ll << 31) || cols >= (1ll << 31)) return MP_ESHAPE;  // 32-bit tile coordinates
   if (n > 0 && (!aligned16(x) || !aligned16(y) || !aligned16(y_t))) return MP_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t *yb = static_cast<uint8_t*>(y), *ytb = static_cast<uint8_t*>(y_t);

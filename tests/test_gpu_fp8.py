@@ -249,6 +249,29 @@ def test_cast_transpose_small(shape, dtype, fmt):
     assert_meta_equal(M.read_fp8_meta(meta), om)
 
 
+@pytest.mark.parametrize("shape,dtype", [((2064, 4112), torch.bfloat16), ((1040, 6160), torch.float32),
+                                         ((4112, 2064), torch.float16)])
+def test_cast_transpose_many_tiles_per_cta(shape, dtype):
+    """Enough 128 x 128 boxes that every CTA's ring of tile copies and its
+    alternating transpose buffers wrap several times, with partial boxes on the
+    right and bottom edges; the amax and the next scale still come out exact."""
+    rows, cols = shape
+    xf = synth.fill(synth.recipe(81, rows, 2.0, 0.01, 80.0, synth.OUT_SCALE), synth.F32, rows * cols)
+    xf[[7, 100_003]] = [np.nan, -np.inf]
+    x = xf if dtype == torch.float32 else O.convert(xf, O.F32, XFMT[dtype])
+    xt = (to_dev(x) if dtype == torch.float32 else to_dev(x, dtype)).reshape(rows, cols)
+    for fmt in (M.MP_E4M3, M.MP_E5M2):
+        meta = M.new_fp8_meta()
+        hist = torch.zeros(4, dtype=torch.float32, device="cuda")
+        set_meta(meta, 0.37)
+        y, yt = cast_t(xt, fmt, meta, hist)
+        ref = O.fp8_cast_array(x, XFMT[dtype], FMT[fmt], 0.37).reshape(rows, cols)
+        assert np.array_equal(y, ref)
+        assert np.array_equal(yt, O.transpose_u8(ref))
+        assert np.isnan(M.read_fp8_meta(meta).amax)
+    assert M.mp_wait_failures() == 0
+
+
 def test_cast_transpose_full_size_sequence():
     c = W.FP8
     meta = M.new_fp8_meta()
