@@ -231,10 +231,82 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
   }
 }
 
-// 16x16 blocks: a CTA covers 16 rows x 256 columns (16 tiles).  Thread t
-// handles row t/16 and the 16-column segment t%16; the tile amax is combined
-// across the two rows a warp holds by shuffle and across warps in shared
-// memory.
+// Encode 8 values of x' (half a 1x16 tile, flat index `flat` a multiple of 8)
+// with block reciprocal r; returns 8 codes, element j in nibble j.  Stochastic
+// rounding takes the 8 random halves of the one Philox call for counter
+// flat / 8, as encode16 does for each half of its tile.
+template <bool SR>
+__device__ __forceinline__ uint32_t encode8(const float (&v)[8], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
+  uint32_t q = 0;
+  if (SR) {
+    const uint64_t g = flat >> 3;
+    const u32x4 R = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
+    const uint32_t words[4] = {R.x, R.y, R.z, R.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t r16 = (j & 1) ? (words[j >> 1] >> 16) : (words[j >> 1] & 0xFFFFu);
+      q |= sr_e2m1(__fmul_rn(v[j], r), r16) << (4 * j);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) q |= cvt_e2m1x2(__fmul_rn(v[2 * k], r), __fmul_rn(v[2 * k + 1], r)) << (8 * k);
+  }
+  return q;
+}
+
+// The 16-point transform of a tile split over a lane pair: the even lane
+// holds elements 0-7, the odd lane 8-15.  The stages of distance 1, 2 and 4
+// stay within a lane; the stage of distance 8 pairs element i of the even
+// lane (a) with element i of the odd lane (b): a + b on the even lane, a - b
+// on the odd one -- the additions of fwht16, in its order.  Then the 1/4.
+__device__ __forceinline__ void fwht16_pair(float (&v)[8], bool odd) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & h) continue;
+      const float a = v[i], b = v[i + h];
+      v[i] = __fadd_rn(a, b);
+      v[i + h] = __fsub_rn(a, b);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], 1);
+    v[i] = odd ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __fmul_rn(v[i], 0.25f);
+}
+
+// x' of a lane's 8 elements (one 16-byte word of BF16).  With the transform
+// every lane of the warp must take part (the pair exchanges values).
+template <bool RHT>
+__device__ __forceinline__ void half_tile_values(uint4 w, uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3,
+                                                 bool odd, float (&v)[8]) {
+  if (RHT) {
+    w.x ^= s0;
+    w.y ^= s1;
+    w.z ^= s2;
+    w.w ^= s3;
+  }
+  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    v[2 * k] = bf16lo(ws[k]);
+    v[2 * k + 1] = bf16hi(ws[k]);
+  }
+  if (RHT) fwht16_pair(v, odd);
+}
+
+// 16x16 blocks: a warp takes a strip of 16 rows x 256 columns (16 blocks) at a
+// time; lane l holds columns 8l .. 8l + 7 of all 16 rows (sixteen 16-byte
+// loads in flight, each row read as 512 consecutive bytes by the warp), so a
+// block is the lane pair (2b, 2b + 1) and its amax takes one shuffle; no CTA
+// barrier.  Each row's 8 codes go out as one 4-byte store (128 bytes per row
+// per warp).  Without the transform the block amax comes from the packed BF16
+// words; with it the values are transformed once for the amax and again for
+// the encode, keeping only the raw words in registers.
 template <bool RHT, bool SR, bool DEQ>
 __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restrict__ x, int64_t rows, int64_t cols,
                                                        uint32_t mask, uint64_t seed,
@@ -242,50 +314,79 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
                                                        const int32_t* __restrict__ nonfinite,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                        uint16_t* __restrict__ deq) {
-  __shared__ float tile_max[8][16];
   const float s_t = *tensor_scale;
   const bool zero = (*nonfinite != 0) || s_t == 0.0f;
   const SignWords sw = sign_words(mask);
   const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-  const int r = threadIdx.x >> 4, seg = threadIdx.x & 15, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const bool odd = lane & 1;
+  const uint32_t s0 = odd ? sw.w[4] : sw.w[0], s1 = odd ? sw.w[5] : sw.w[1];
+  const uint32_t s2 = odd ? sw.w[6] : sw.w[2], s3 = odd ? sw.w[7] : sw.w[3];
   const int64_t ncc = (cols + 255) / 256;
   const int64_t nitems = (rows / 16) * ncc;
   const int64_t nb = cols / 16;
-  for (int64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+  const int64_t warps = (int64_t)gridDim.x * (kThreads / 32);
+  for (int64_t item = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); item < nitems; item += warps) {
     const int64_t tr = item / ncc, cc = item % ncc;
-    const int64_t row = tr * 16 + r;
-    const int64_t col = cc * 256 + seg * 16;
-    const bool active = col < cols;
-    const int64_t flat = row * cols + col;
-    float v[16];
-    float m = 0.0f;
-    if (active && !zero) {
-      load_tile<RHT>(x + flat, sw, v);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
-    }
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    if ((threadIdx.x & 31) < 16) tile_max[warp][seg] = m;
-    __syncthreads();
-    float bamax = tile_max[0][seg];
-#pragma unroll
-    for (int w = 1; w < 8; ++w) bamax = fmaxf(bamax, tile_max[w][seg]);
-    __syncthreads();  // tile_max is rewritten by the next item
-    if (!active) continue;
+    const int64_t col = cc * 256 + lane * 8;
+    const bool active = col < cols;  // cols % 16 == 0: both lanes of a pair agree
+    const int64_t base = tr * 16 * cols + col;
     if (zero) {
-      *reinterpret_cast<uint2*>(codes + flat / 2) = make_uint2(0u, 0u);
-      if (r == 0) scales[tr * nb + col / 16] = 0;
-      if (DEQ) {
-        st_cs(deq + flat, make_uint4(0u, 0u, 0u, 0u));
-        st_cs(deq + flat + 8, make_uint4(0u, 0u, 0u, 0u));
+      if (!active) continue;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        *reinterpret_cast<uint32_t*>(codes + (base + r * cols) / 2) = 0u;
+        if (DEQ) st_cs(deq + base + r * cols, make_uint4(0u, 0u, 0u, 0u));
       }
+      if (!odd) scales[tr * nb + col / 16] = 0;
       continue;
     }
+    uint4 raw[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) raw[r] = active ? ld_plain(x + base + r * cols) : make_uint4(0u, 0u, 0u, 0u);
+    float m;
+    if (!RHT) {
+      uint32_t acc[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        acc[0] = max_abs_nan_x2<true>(acc[0], raw[r].x);
+        acc[1] = max_abs_nan_x2<true>(acc[1], raw[r].y);
+        acc[2] = max_abs_nan_x2<true>(acc[2], raw[r].z);
+        acc[3] = max_abs_nan_x2<true>(acc[3], raw[r].w);
+      }
+      const uint32_t p = max_abs_nan_x2<true>(max_abs_nan_x2<true>(acc[0], acc[1]), max_abs_nan_x2<true>(acc[2], acc[3]));
+      m = fmaxf(bf16lo(p), bf16hi(p));
+    } else {
+      m = 0.0f;
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        float v[8];
+        half_tile_values<true>(raw[r], s0, s1, s2, s3, odd, v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+      }
+    }
+    const float bamax = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
     const BlockScale bs = block_scale(bamax, s_t);
-    const uint2 q = encode16<SR>(v, bs.r, (uint64_t)flat, k0, k1);
-    __stcs(reinterpret_cast<uint2*>(codes + flat / 2), q);
-    if (r == 0) scales[tr * nb + col / 16] = (uint8_t)bs.code;
-    if (DEQ) dequant16(q, bs.d, deq + flat);
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float v[8];
+      half_tile_values<RHT>(raw[r], s0, s1, s2, s3, odd, v);
+      if (!active) continue;
+      const uint64_t flat = (uint64_t)(base + r * cols);
+      const uint32_t q = encode8<SR>(v, bs.r, flat, k0, k1);
+      __stcs(reinterpret_cast<uint32_t*>(codes + flat / 2), q);
+      if (DEQ) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t byte = (q >> (8 * k)) & 0xFFu;
+          w[k] = pack_bf16x2(__fmul_rn(e2m1_to_f32(byte & 0xFu), bs.d), __fmul_rn(e2m1_to_f32(byte >> 4), bs.d));
+        }
+        st_cs(deq + flat, make_uint4(w[0], w[1], w[2], w[3]));
+      }
+    }
+    if (active && !odd) scales[tr * nb + col / 16] = (uint8_t)bs.code;
   }
 }
 
@@ -350,9 +451,10 @@ void launch_encode(bool block_2d, const uint16_t* x, int64_t rows, int64_t cols,
                    cudaStream_t s) {
   if (block_2d) {
     static const int occ = occ_of(k_nvfp4_2d<RHT, SR, DEQ>);
-    const int64_t items = (rows / 16) * ((cols + 255) / 256);
-    k_nvfp4_2d<RHT, SR, DEQ><<<grid_for(items, occ), kThreads, 0, s>>>(x, rows, cols, mask, seed, ts, nf, codes,
-                                                                        scales, deq);
+    const int64_t items = (rows / 16) * ((cols + 255) / 256);  // one warp each
+    const int64_t ctas = (items + kThreads / 32 - 1) / (kThreads / 32);
+    k_nvfp4_2d<RHT, SR, DEQ><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, rows, cols, mask, seed, ts, nf, codes,
+                                                                       scales, deq);
   } else {
     static const int occ = occ_of(k_nvfp4_1x16<RHT, SR, DEQ>);
     const int64_t nblocks = rows * (cols / 16);
