@@ -282,8 +282,8 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // ---------------------------------------------------------------------------
 // 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
 // a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
-// shared-memory stages (kRingBytes: six 32 KB stages for 16-bit input, three
-// 64 KB for FP32).  The consumers are kGroups groups of eight warps; group g
+// shared-memory stages (six 32 KB stages for 16-bit input, two 64 KB for
+// FP32).  The consumers are kGroups groups of eight warps; group g
 // takes the CTA's rounds g, g + kGroups, ..., so several blocks are reduced
 // and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
 // elements) of the stage into registers and releases the stage at once, so
@@ -301,17 +301,26 @@ constexpr int kRingBytes = 192 * 1024;
 
 __device__ unsigned int g_wait_failures;  // bounded waits that gave up (read by mp_wait_failures)
 
+// Ring stage s is filled for the CTA's rounds s, s + kStages, ...; group g
+// takes rounds g, g + kGroups, ...  With kStages a multiple of kGroups every
+// stage belongs to one group, which waits for the stage's fills in order, so a
+// parity wait can never match a phase two fills old.  (A stage shared by two
+// groups would let one group run a fill ahead of the other, see the previous
+// fill's parity and read stale bytes, and its early arrivals would let the
+// producer re-arm a barrier whose phase has not completed.)
 template <int XT>
 struct BlkGeom {
   static constexpr int kEs = XT == XF32 ? 4 : 2;                 // input element bytes
   static constexpr int kG = 16 / kEs;                             // elements per 16-byte group
   static constexpr int kStage = 128 * 128 * kEs;                  // one block
-  static constexpr int kStages = kRingBytes / kStage;             // 6 or 3
-  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 16-byte groups per consumer thread: 8 or 16
   static constexpr int kGroups = XT == XF32 ? 2 : 3;              // consumer groups (register budget)
+  static constexpr int kStages = XT == XF32 ? 2 : 6;              // 128 KB or 192 KB of ring
+  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 16-byte groups per consumer thread: 8 or 16
   static constexpr int kThreads = kGroups * kGroupThreads + 32;   // + the producer warp
   static constexpr size_t kSmem = (size_t)kStages * kStage + 2 * kStages * sizeof(uint64_t) +
                                   (size_t)kGroups * 2 * kGroupWarps * sizeof(uint32_t);
+  static_assert(kStages % kGroups == 0, "every ring stage must belong to one consumer group");
+  static_assert(kStages * kStage <= kRingBytes, "ring larger than its budget");
 };
 
 // One 16-byte group of raw input (8 16-bit or 4 FP32 elements) cast with
@@ -585,8 +594,8 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
 
 // ---------------------------------------------------------------------------
 // Cast + transposed copy through the tensor-copy engine: the same producer and
-// 128 x 128 boxes as above, a 128 KB ring (four 32 KB stages, or two 64 KB for
-// FP32) and kGroups consumer groups on alternate boxes.  A group casts its box
+// 128 x 128 boxes as above, a ring of one stage per consumer group (three
+// 32 KB stages, or two 64 KB for FP32) and kGroups groups on alternate boxes.  A group casts its box
 // from registers with the delayed scale, writes y directly and the same bytes
 // row-major into its own 16 KB shared tile (two per group, alternating by
 // round, so one named barrier per round suffices), then reads the tile back a
@@ -599,13 +608,15 @@ struct TrGeom {
   static constexpr int kEs = XT == XF32 ? 4 : 2;
   static constexpr int kG = 16 / kEs;
   static constexpr int kStage = 128 * 128 * kEs;
-  static constexpr int kStages = (128 * 1024) / kStage;          // 4 or 2
-  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 8 or 16
   static constexpr int kGroups = XT == XF32 ? 2 : 3;
+  static constexpr int kStages = XT == XF32 ? 2 : 3;              // one stage per group (see BlkGeom)
+  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 8 or 16
   static constexpr int kThreads = kGroups * kGroupThreads + 32;
   static constexpr int kTile = 128 * 128;                         // cast bytes of one box
   static constexpr size_t kSmem = (size_t)kStages * kStage + (size_t)kGroups * 2 * kTile +
                                   2 * kStages * sizeof(uint64_t) + (size_t)kGroups * kGroupWarps * sizeof(uint32_t);
+  static_assert(kStages % kGroups == 0, "every ring stage must belong to one consumer group");
+  static_assert(kSmem <= 227 * 1024, "shared memory beyond the per-CTA limit");
 };
 
 template <int XT, bool E5M2>
