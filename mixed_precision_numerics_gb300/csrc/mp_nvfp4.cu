@@ -54,6 +54,54 @@ __device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw
   tile_values<RHT>(ld_plain(p), ld_plain(p + 8), sw, v);
 }
 
+// The 16-point butterfly of fwht16 in packed binary32 arithmetic.  The tile
+// is held as eight pairs p[i] = (v[i], v[i + 8]): the stages of distance 1, 2
+// and 4 pair element i with i + h in both halves at once, so one packed add
+// gives both sums and one packed fma(b, -1, a) both differences (the product
+// by -1 is exact, so the fma rounds a - b once, as the subtraction does); the
+// stage of distance 8 works inside each pair.  Every element receives
+// fwht16's additions in its order, each rounded as there.
+__device__ __forceinline__ void fwht16_packed(float2 (&p)[8]) {
+  const float2 m1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i & h) continue;
+      const float2 a = p[i], b = p[i + h];
+      p[i] = __fadd2_rn(a, b);
+      p[i + h] = __ffma2_rn(b, m1, a);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float a = p[i].x, b = p[i].y;
+    p[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
+  }
+}
+
+// x' of one 16-element BF16 tile (two 16-byte words) as the pairs
+// (x'[i], x'[i + 8]); `quarter` applies the transform's 1/4 (the amax pass
+// applies it once to the maximum instead).
+template <bool RHT, bool QUARTER = true>
+__device__ __forceinline__ void tile_pairs(uint4 a, uint4 b, const SignWords& sw, float2 (&p)[8]) {
+  if (RHT) apply_signs(a, b, sw);
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float lo = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+    const float hi = (i & 1) ? bf16hi(w[4 + (i >> 1)]) : bf16lo(w[4 + (i >> 1)]);
+    p[i] = make_float2(lo, hi);
+  }
+  if (RHT) {
+    fwht16_packed(p);
+    if (QUARTER) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) p[i] = __fmul2_rn(p[i], make_float2(0.25f, 0.25f));
+    }
+  }
+}
+
 template <bool RHT>
 __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restrict__ x, int64_t ntiles,
                                                          uint32_t mask, Ws* ws, float* tensor_scale,
@@ -84,12 +132,13 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restr
     for (int u = 0; u < U; ++u) {
       const int64_t t = t0 + (int64_t)u * kThreads;
       if (t >= ntiles) continue;
-      if (RHT) apply_signs(a[u], b[u], sw);
-      float v[16];
-      unpack_bf16x16(a[u], b[u], v);
-      if (RHT) fwht16(v);  // the 1/4 is applied once to the maximum below
+      float2 p[8];
+      tile_pairs<RHT, false>(a[u], b[u], sw, p);  // the 1/4 is applied once to the maximum below
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc = max_abs_nan(acc, v[j]);
+      for (int j = 0; j < 8; ++j) {
+        acc = max_abs_nan(acc, p[j].x);
+        acc = max_abs_nan(acc, p[j].y);
+      }
     }
   }
   const uint32_t cta = block_max_u32(amax_bits(acc), red);
@@ -181,6 +230,44 @@ __device__ __forceinline__ uint2 encode16(const float (&v)[16], float r, uint64_
   return make_uint2(lo, hi);
 }
 
+// encode16 for a tile held as pairs (x'[i], x'[i + 8]); the products x' * r
+// are formed two at a time (packed binary32 multiply, each rounded as
+// __fmul_rn).
+template <bool SR>
+__device__ __forceinline__ uint2 encode16p(const float2 (&p)[8], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
+  float y[16];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 q = __fmul2_rn(p[i], make_float2(r, r));
+    y[i] = q.x;
+    y[i + 8] = q.y;
+  }
+  uint32_t lo = 0, hi = 0;
+  if (SR) {
+    const uint64_t g = flat >> 3;
+    const u32x4 R0 = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
+    const uint64_t g1 = g + 1;
+    const u32x4 R1 = philox4x32_10((uint32_t)g1, (uint32_t)(g1 >> 32), 0u, 0u, k0, k1);
+    const uint32_t words[8] = {R0.x, R0.y, R0.z, R0.w, R1.x, R1.y, R1.z, R1.w};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t w = words[j >> 1];
+      const uint32_t r16 = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
+      const uint32_t c = sr_e2m1(y[j], r16);
+      if (j < 8) lo |= c << (4 * j);
+      else hi |= c << (4 * (j - 8));
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t c = cvt_e2m1x2(y[2 * k], y[2 * k + 1]);
+      if (k < 4) lo |= c << (8 * k);
+      else hi |= c << (8 * (k - 4));
+    }
+  }
+  return make_uint2(lo, hi);
+}
+
 // BF16 RNE of value(code) * d for the 16 codes in (lo, hi).
 __device__ __forceinline__ void dequant16(uint2 q, float d, uint16_t* out) {
   uint32_t w[8];
@@ -218,13 +305,13 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
       }
       continue;
     }
-    float v[16];
-    tile_values<RHT>(ld_hint(x + blk * 16, last_use), ld_hint(x + blk * 16 + 8, last_use), sw, v);
+    float2 p[8];
+    tile_pairs<RHT>(ld_hint(x + blk * 16, last_use), ld_hint(x + blk * 16 + 8, last_use), sw, p);
     float bamax = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) bamax = fmaxf(bamax, fabsf(v[j]));
+    for (int j = 0; j < 8; ++j) bamax = fmaxf(bamax, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
     const BlockScale bs = block_scale(bamax, s_t);
-    const uint2 q = encode16<SR>(v, bs.r, (uint64_t)blk * 16, k0, k1);
+    const uint2 q = encode16p<SR>(p, bs.r, (uint64_t)blk * 16, k0, k1);
     __stcs(reinterpret_cast<uint2*>(codes + blk * 8), q);
     scales[blk] = (uint8_t)bs.code;
     if (DEQ) dequant16(q, bs.d, deq + blk * 16);
