@@ -187,17 +187,20 @@ __device__ __forceinline__ BlockScale block_scale(float bamax, float s_t) {
 }
 
 // Stochastic E2M1 code of y with 16 random bits: round away from zero iff
-// floor(frac * 2^16) + r16 >= 2^16.  For |y| >= 1 the 22 fraction bits below
-// the kept mantissa bit of |y| are exactly frac * 2^22; for |y| < 1 the same
-// holds for the bits of 1 + |y| truncated to binary32.  Adding r16 at bit 6
-// carries into bit 22 exactly when the rule rounds up.
+// floor(frac * 2^16) + r16 >= 2^16.  For a = |y| >= 1 the 22 fraction bits
+// below the kept mantissa bit of a are exactly frac * 2^22; for a < 1 the same
+// holds for the bits of 1 + a truncated to binary32, here halved to
+// (1 + a) / 2 (an exact scaling, so the same fraction bits one exponent step
+// lower), which lets one offset serve both ranges: with b the chosen value,
+// ((bits(b) + r16 * 2^6) >> 22) - 252 is the magnitude code, the add carrying
+// into bit 22 exactly when the rule rounds up.  b needs no branch:
+// fma_rz(a, 0.5, 0.5) = RZ((1 + a) / 2) exceeds a for a < 1 and is at most a
+// for a >= 1 (where it equals a only at a = 1), so b = max(a, it).
 __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r16) {
   const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
   const float a = fminf(fabsf(y), 6.0f);
-  const bool sub = a < 1.0f;
-  const float b = sub ? __fadd_rz(a, 1.0f) : a;
-  const uint32_t adj = sub ? (254u << 22) : (252u << 22);
-  return (((__float_as_uint(b) + (r16 << 6)) - adj) >> 22) | sign;
+  const float b = fmaxf(a, __fmaf_rz(a, 0.5f, 0.5f));
+  return (((__float_as_uint(b) + r16 * 64u) >> 22) - 252u) | sign;
 }
 
 // Encode 16 values of x' with block reciprocal r; returns 8 packed bytes.
