@@ -200,7 +200,7 @@ __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r16) {
   const uint32_t sign = (__float_as_uint(y) >> 28) & 8u;
   const float a = fminf(fabsf(y), 6.0f);
   const float b = fmaxf(a, __fmaf_rz(a, 0.5f, 0.5f));
-  return (((__float_as_uint(b) + r16 * 64u) >> 22) - 252u) | sign;
+  return (((__float_as_uint(b) + r16 * 64u) >> 22) - 252u) + sign;  // magnitude <= 7: + is |
 }
 
 // Encode 16 values of x' with block reciprocal r; returns 8 packed bytes.
@@ -257,8 +257,8 @@ __device__ __forceinline__ uint2 encode16p(const float2 (&p)[8], float r, uint64
       const uint32_t w = words[j >> 1];
       const uint32_t r16 = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
       const uint32_t c = sr_e2m1(y[j], r16);
-      if (j < 8) lo |= c << (4 * j);
-      else hi |= c << (4 * (j - 8));
+      if (j < 8) lo += c << (4 * j);  // disjoint nibbles: + is |
+      else hi += c << (4 * (j - 8));
     }
   } else {
 #pragma unroll
