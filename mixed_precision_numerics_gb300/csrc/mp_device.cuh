@@ -179,33 +179,6 @@ __device__ __forceinline__ void apply_signs(uint4& a, uint4& b, const SignWords&
 }
 
 // ---------------------------------------------------------------------------
-// 16-point Walsh-Hadamard butterfly in registers, spans 1, 2, 4, 8:
-// v <- H16 v with H16[i][j] = (-1)^popcount(i & j).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void fwht16(float (&v)[16]) {
-#pragma unroll
-  for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i & h) continue;
-      const float a = v[i], b = v[i + h];
-      v[i] = __fadd_rn(a, b);
-      v[i + h] = __fsub_rn(a, b);
-    }
-  }
-}
-
-// Unpack 16 BF16 values from two 16-byte words.
-__device__ __forceinline__ void unpack_bf16x16(uint4 a, uint4 b, float (&v)[16]) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    v[2 * k] = bf16lo(w[k]);
-    v[2 * k + 1] = bf16hi(w[k]);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Bulk asynchronous copies (TMA engine, cp.async.bulk) and mbarriers.
 // Every wait is bounded: at most kWaitLimit polls, each suspending for at
 // most kWaitSuspendNs, so a wait gives up after about two seconds and the

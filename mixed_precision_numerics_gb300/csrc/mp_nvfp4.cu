@@ -36,31 +36,15 @@ struct Ws {
   uint32_t ticket;
 };
 
-// x' in binary32 of one 16-element BF16 tile given as two 16-byte words.
-template <bool RHT>
-__device__ __forceinline__ void tile_values(uint4 a, uint4 b, const SignWords& sw, float (&v)[16]) {
-  if (RHT) apply_signs(a, b, sw);
-  unpack_bf16x16(a, b, v);
-  if (RHT) {
-    fwht16(v);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
-  }
-}
-
-// Load one 16-element tile of BF16 and produce x' in binary32.
-template <bool RHT>
-__device__ __forceinline__ void load_tile(const uint16_t* p, const SignWords& sw, float (&v)[16]) {
-  tile_values<RHT>(ld_plain(p), ld_plain(p + 8), sw, v);
-}
-
-// The 16-point butterfly of fwht16 in packed binary32 arithmetic.  The tile
-// is held as eight pairs p[i] = (v[i], v[i + 8]): the stages of distance 1, 2
+// The 16-point Walsh-Hadamard butterfly, v <- H16 v with H16[i][j] =
+// (-1)^popcount(i & j): stages of distance h = 1, 2, 4, 8, each replacing
+// (v[i], v[i + h]) for i with bit h clear by (a + b, a - b), every operation a
+// binary32 add rounded to nearest even.  Here in packed arithmetic: the tile
+// is held as eight pairs p[i] = (v[i], v[i + 8]); the stages of distance 1, 2
 // and 4 pair element i with i + h in both halves at once, so one packed add
 // gives both sums and one packed fma(b, -1, a) both differences (the product
 // by -1 is exact, so the fma rounds a - b once, as the subtraction does); the
-// stage of distance 8 works inside each pair.  Every element receives
-// fwht16's additions in its order, each rounded as there.
+// stage of distance 8 works inside each pair.
 __device__ __forceinline__ void fwht16_packed(float2 (&p)[8]) {
   const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
@@ -203,39 +187,10 @@ __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r16) {
   return (((__float_as_uint(b) + r16 * 64u) >> 22) - 252u) + sign;  // magnitude <= 7: + is |
 }
 
-// Encode 16 values of x' with block reciprocal r; returns 8 packed bytes.
-// `flat` is the flat index of the first element (a multiple of 16).
-template <bool SR>
-__device__ __forceinline__ uint2 encode16(const float (&v)[16], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
-  uint32_t lo = 0, hi = 0;
-  if (SR) {
-    const uint64_t g = flat >> 3;
-    const u32x4 R0 = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
-    const uint64_t g1 = g + 1;
-    const u32x4 R1 = philox4x32_10((uint32_t)g1, (uint32_t)(g1 >> 32), 0u, 0u, k0, k1);
-    const uint32_t words[8] = {R0.x, R0.y, R0.z, R0.w, R1.x, R1.y, R1.z, R1.w};
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t w = words[j >> 1];
-      const uint32_t r16 = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-      const uint32_t c = sr_e2m1(__fmul_rn(v[j], r), r16);
-      if (j < 8) lo |= c << (4 * j);
-      else hi |= c << (4 * (j - 8));
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t c = cvt_e2m1x2(__fmul_rn(v[2 * k], r), __fmul_rn(v[2 * k + 1], r));
-      if (k < 4) lo |= c << (8 * k);
-      else hi |= c << (8 * (k - 4));
-    }
-  }
-  return make_uint2(lo, hi);
-}
-
-// encode16 for a tile held as pairs (x'[i], x'[i + 8]); the products x' * r
-// are formed two at a time (packed binary32 multiply, each rounded as
-// __fmul_rn).
+// Encode a 16-element tile of x', held as pairs (x'[i], x'[i + 8]), with block
+// reciprocal r; returns 8 packed bytes.  The products x' * r are formed two at
+// a time (packed binary32 multiply, each rounded as __fmul_rn).  `flat` is the
+// flat index of the first element (a multiple of 16).
 template <bool SR>
 __device__ __forceinline__ uint2 encode16p(const float2 (&p)[8], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
   float y[16];
@@ -348,7 +303,7 @@ __device__ __forceinline__ uint32_t encode8(const float (&v)[8], float r, uint64
 // holds elements 0-7, the odd lane 8-15.  The stages of distance 1, 2 and 4
 // stay within a lane; the stage of distance 8 pairs element i of the even
 // lane (a) with element i of the odd lane (b): a + b on the even lane, a - b
-// on the odd one -- the additions of fwht16, in its order.  Then the 1/4.
+// on the odd one -- the butterfly's additions, in its order.  Then the 1/4.
 __device__ __forceinline__ void fwht16_pair(float (&v)[8], bool odd) {
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1) {
@@ -486,19 +441,20 @@ __global__ __launch_bounds__(kThreads) void k_rht16(const uint16_t* __restrict__
   const SignWords sw = sign_words(mask);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < ntiles; t += stride) {
-    float v[16];
-    load_tile<true>(x + t * 16, sw, v);
+    float2 p[8];  // (x'[i], x'[i + 8])
+    tile_pairs<true>(ld_plain(x + t * 16), ld_plain(x + t * 16 + 8), sw, p);
     if (F32OUT) {
       float* o = static_cast<float*>(y) + t * 16;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) st_cs_f4(o + 4 * k, make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]));
+      st_cs_f4(o, make_float4(p[0].x, p[1].x, p[2].x, p[3].x));
+      st_cs_f4(o + 4, make_float4(p[4].x, p[5].x, p[6].x, p[7].x));
+      st_cs_f4(o + 8, make_float4(p[0].y, p[1].y, p[2].y, p[3].y));
+      st_cs_f4(o + 12, make_float4(p[4].y, p[5].y, p[6].y, p[7].y));
     } else {
       uint16_t* o = static_cast<uint16_t*>(y) + t * 16;
-      uint32_t w[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
-      st_cs(o, make_uint4(w[0], w[1], w[2], w[3]));
-      st_cs(o + 8, make_uint4(w[4], w[5], w[6], w[7]));
+      st_cs(o, make_uint4(pack_bf16x2(p[0].x, p[1].x), pack_bf16x2(p[2].x, p[3].x), pack_bf16x2(p[4].x, p[5].x),
+                          pack_bf16x2(p[6].x, p[7].x)));
+      st_cs(o + 8, make_uint4(pack_bf16x2(p[0].y, p[1].y), pack_bf16x2(p[2].y, p[3].y),
+                              pack_bf16x2(p[4].y, p[5].y), pack_bf16x2(p[6].y, p[7].y)));
     }
   }
 }
