@@ -12,6 +12,13 @@
 // folds a small slice of the history entries the call does not overwrite into
 // a second word; the last CTA to finish (atomic ticket, no waiting) writes the
 // ring slot and derives the next scale from the two maxima.
+//
+// The 2-D tile casts -- the cast with a transposed copy (k_fp8_cast_t_tma)
+// and the fine-grained casts with 1x128 or 128x128 block scales
+// (k_fp8_block_tma) -- read 128 x 128 boxes through 2-D tensor copies into a
+// shared-memory ring that one producer lane keeps full, consumed by groups of
+// eight warps; each wait is bounded and a wait that gives up is counted for
+// mp_wait_failures.
 #include <string.h>
 
 #include "mp_device.cuh"
