@@ -133,6 +133,30 @@ def _check(fn: str, status: int) -> None:
         raise MpError(fn, status)
 
 
+def _dev(t, name: str, nbytes: int = 0, like=None, align: int = 16) -> None:
+    """Checks a tensor before its pointer crosses the C ABI, which cannot tell
+    host from device memory: it must live on the CUDA device the call runs on
+    (the current device, or that of `like`), be contiguous, and hold at least
+    `nbytes`.  The size is not checked when the pointer breaks the argument's
+    alignment rule (`align` bytes): the library reports that itself, before
+    any launch.  Raw integer pointers and None pass unchecked."""
+    if t is None or isinstance(t, int):
+        return
+    import torch
+
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"{name}: a CUDA tensor is required (the kernels read and write device memory)")
+    want = like.device if like is not None and not isinstance(like, int) else torch.device(
+        "cuda", torch.cuda.current_device())
+    if t.device != want:
+        raise ValueError(f"{name}: on {t.device}, the call runs on {want}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: a contiguous tensor is required")
+    have = t.numel() * t.element_size()
+    if t.data_ptr() % align == 0 and have < nbytes:
+        raise ValueError(f"{name}: {have} bytes, the call needs {nbytes}")
+
+
 def _ptr(t) -> int | None:
     if t is None:
         return None
@@ -233,6 +257,12 @@ class Param:
 
 
 def make_param_array(params: Sequence[Param]):
+    for i, p in enumerate(params):
+        n = p.master.numel() if not isinstance(p.master, int) else 0
+        ref = params[0].master
+        for name, t, es in (("master", p.master, 4), ("exp_avg", p.exp_avg, 4), ("exp_avg_sq", p.exp_avg_sq, 4),
+                            ("grad", p.grad, 2), ("working", p.working, 2)):
+            _dev(t, f"params[{i}].{name}", n * es, like=ref)
     arr = (MpParam * max(1, len(params)))()
     for i, p in enumerate(params):
         arr[i] = MpParam(_ptr(p.master), _ptr(p.exp_avg), _ptr(p.exp_avg_sq), _ptr(p.grad), _ptr(p.working),
@@ -257,6 +287,8 @@ def mp_adamw_step(params, hp: AdamwHparams, state, grad_dtype: int | None = None
     dtypes).  workspace: device buffer of mp_adamw_workspace_size bytes, needed
     only when hp.max_grad_norm > 0."""
     arr, n, g, w = _marshal(params, grad_dtype, working_dtype)
+    _dev(state, "state", ctypes.sizeof(ScalerState), align=8)
+    _dev(workspace, "workspace", align=8)
     wp, wb = _ws(workspace)
     _check("mp_adamw_step", lib.mp_adamw_step(arr, n, g, w, ctypes.byref(hp), _ptr(state), wp, wb, _stream(stream)))
 
@@ -278,6 +310,8 @@ def _marshal(params, grad_dtype, working_dtype):
 def mp_adamw_check(params, hp: AdamwHparams, state, grad_dtype: int | None = None, workspace=None,
                    stream=None) -> None:
     arr, n, g, _ = _marshal(params, grad_dtype, MP_F16 if grad_dtype is not None else None)
+    _dev(state, "state", ctypes.sizeof(ScalerState), align=8)
+    _dev(workspace, "workspace", align=8)
     wp, wb = _ws(workspace)
     _check("mp_adamw_check", lib.mp_adamw_check(arr, n, g, ctypes.byref(hp), _ptr(state), wp, wb, _stream(stream)))
 
@@ -285,10 +319,12 @@ def mp_adamw_check(params, hp: AdamwHparams, state, grad_dtype: int | None = Non
 def mp_adamw_apply(params, hp: AdamwHparams, state, grad_dtype: int | None = None,
                    working_dtype: int | None = None, stream=None) -> None:
     arr, n, g, w = _marshal(params, grad_dtype, working_dtype)
+    _dev(state, "state", ctypes.sizeof(ScalerState), align=8)
     _check("mp_adamw_apply", lib.mp_adamw_apply(arr, n, g, w, ctypes.byref(hp), _ptr(state), _stream(stream)))
 
 
 def loss_scale_update(state, cfg: ScalerCfg, stream=None) -> None:
+    _dev(state, "state", ctypes.sizeof(ScalerState), align=8)
     _check("loss_scale_update", lib.loss_scale_update(_ptr(state), ctypes.byref(cfg), _stream(stream)))
 
 
@@ -298,16 +334,30 @@ MP_AMAX_HISTORY_MAX, MP_AMAX_MOST_RECENT = 0, 1
 def fp8_cast_delayed(x, y, fp8_dtype: int, meta, history, margin: float = 1.0, stream=None,
                      n: int | None = None, amax_algo: int = MP_AMAX_HISTORY_MAX) -> None:
     """y: uint8 (or float8) tensor with x.numel() elements; history: float32 device tensor."""
+    ne = x.numel() if n is None else n
+    _fp8_args(x, y, ne, meta, history)
     _check("fp8_cast_delayed",
            lib.fp8_cast_delayed(_ptr(x), _dtype_code(x), x.numel() if n is None else n, _ptr(y), fp8_dtype,
                                 _ptr(meta), _ptr(history), history.numel(), float(margin), amax_algo,
                                 _stream(stream)))
 
 
+def _fp8_args(x, y, n, meta, history, y_t=None):
+    if isinstance(x, int):
+        return
+    _dev(x, "x", n * x.element_size())
+    _dev(y, "y", n, like=x)
+    _dev(y_t, "y_t", n, like=x)
+    _dev(meta, "meta", ctypes.sizeof(Fp8Meta), like=x)
+    _dev(history, "history", 4, like=x, align=4)
+
+
 def fp8_cast_delayed_count(x, y, fp8_dtype: int, meta, history, saturated, margin: float = 1.0,
                            amax_algo: int = MP_AMAX_HISTORY_MAX, stream=None) -> None:
     """fp8_cast_delayed that also adds the number of saturated elements to
     `saturated` (an int64 device tensor of one element)."""
+    _fp8_args(x, y, x.numel(), meta, history)
+    _dev(saturated, "saturated", 8, like=x, align=8)
     _check("fp8_cast_delayed_count",
            lib.fp8_cast_delayed_count(_ptr(x), _dtype_code(x), x.numel(), _ptr(y), fp8_dtype, _ptr(meta),
                                       _ptr(history), history.numel(), float(margin), amax_algo, _ptr(saturated),
@@ -318,6 +368,7 @@ def fp8_cast_transpose_delayed(x, y, y_t, fp8_dtype: int, meta, history, margin:
                                amax_algo: int = MP_AMAX_HISTORY_MAX, stream=None) -> None:
     """x: [rows, cols]; y: rows*cols bytes; y_t: cols*rows bytes (the transpose)."""
     rows, cols = x.shape
+    _fp8_args(x, y, rows * cols, meta, history, y_t)
     _check("fp8_cast_transpose_delayed",
            lib.fp8_cast_transpose_delayed(_ptr(x), _dtype_code(x), rows, cols, _ptr(y), _ptr(y_t), fp8_dtype,
                                           _ptr(meta), _ptr(history), history.numel(), float(margin), amax_algo,
@@ -328,9 +379,27 @@ def fp8_quantize_blockwise(x, y, scales, block_rows: int = 1, block_cols: int = 
                            stream=None) -> None:
     """x: [rows, cols]; y: rows*cols bytes; scales: float32 [ceil(rows/br), ceil(cols/bc)]."""
     rows, cols = x.shape
+    _dev(x, "x", rows * cols * x.element_size())
+    _dev(y, "y", rows * cols, like=x)
+    if (block_rows, block_cols) in ((1, 128), (128, 128)):
+        _dev(scales, "scales", 4 * (-(-rows // block_rows)) * (-(-cols // block_cols)), like=x, align=4)
+    else:
+        _dev(scales, "scales", like=x, align=4)
     _check("fp8_quantize_blockwise",
            lib.fp8_quantize_blockwise(_ptr(x), _dtype_code(x), rows, cols, block_rows, block_cols, _ptr(y), fp8_dtype,
                                       _ptr(scales), _stream(stream)))
+
+
+def _nvfp4_args(x, codes, block_scales, tensor_scale, nonfinite, dequant, rows, cols, block_2d):
+    n = rows * cols
+    _dev(x, "x", 2 * n)
+    _dev(codes, "codes", n // 2, like=x)
+    shape_ok = cols % 16 == 0 and (not block_2d or rows % 16 == 0)
+    _dev(block_scales, "block_scales", ((rows // 16 if block_2d else rows) * (cols // 16)) if shape_ok else 0,
+         like=x, align=1)
+    _dev(tensor_scale, "tensor_scale", 4, like=x, align=4)
+    _dev(nonfinite, "nonfinite", 4, like=x, align=4)
+    _dev(dequant, "dequant", 2 * n, like=x)
 
 
 def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *, block_2d: bool = False,
@@ -338,6 +407,8 @@ def nvfp4_quantize(x, codes, block_scales, tensor_scale, nonfinite, workspace, *
                    dequant=None, rows: int | None = None, cols: int | None = None, stream=None) -> None:
     if rows is None:
         rows, cols = x.shape
+    _nvfp4_args(x, codes, block_scales, tensor_scale, nonfinite, dequant, rows, cols, block_2d)
+    _dev(workspace, "workspace", like=x, align=8)
     _check("nvfp4_quantize",
            lib.nvfp4_quantize(_ptr(x), rows, cols, int(block_2d), int(stochastic), seed & (2**64 - 1),
                               int(apply_rht), sign_mask & 0xFFFF, _ptr(codes), _ptr(block_scales),
@@ -353,6 +424,7 @@ def nvfp4_quantize_noalloc(x, codes, block_scales, tensor_scale, nonfinite, *, b
     on the GPU race on it; see the C header)."""
     if rows is None:
         rows, cols = x.shape
+    _nvfp4_args(x, codes, block_scales, tensor_scale, nonfinite, dequant, rows, cols, block_2d)
     _check("nvfp4_quantize_noalloc",
            lib.nvfp4_quantize_noalloc(_ptr(x), rows, cols, int(block_2d), int(stochastic), seed & (2**64 - 1),
                                       int(apply_rht), sign_mask & 0xFFFF, _ptr(codes), _ptr(block_scales),
@@ -361,6 +433,9 @@ def nvfp4_quantize_noalloc(x, codes, block_scales, tensor_scale, nonfinite, *, b
 
 def rht16(x, y, sign_mask: int, stream=None) -> None:
     rows, cols = x.shape
+    _dev(x, "x", 2 * rows * cols)
+    if not isinstance(y, int):
+        _dev(y, "y", rows * cols * y.element_size(), like=x)
     _check("rht16", lib.rht16(_ptr(x), rows, cols, sign_mask & 0xFFFF, _ptr(y), _dtype_code(y), _stream(stream)))
 
 
@@ -368,6 +443,12 @@ def mx_quantize(x, codes, scales, elem_dtype: int = MP_E2M1, dequant=None, strea
     """x: [rows, cols], cols % 32 == 0; codes: rows*cols bytes (FP8, FP6) or
     rows*cols/2 (E2M1); scales: uint8 [rows, cols/32] (UE8M0)."""
     rows, cols = x.shape
+    n = rows * cols
+    ok = cols % 32 == 0 and elem_dtype in (MP_E4M3, MP_E5M2, MP_E2M1, MP_E2M3, MP_E3M2)  # else the library says why
+    _dev(x, "x", n * x.element_size())
+    _dev(codes, "codes", (n // 2 if elem_dtype == MP_E2M1 else n) if ok else 0, like=x)
+    _dev(scales, "scales", n // 32 if ok else 0, like=x, align=1)
+    _dev(dequant, "dequant", 2 * n if ok else 0, like=x)
     _check("mx_quantize", lib.mx_quantize(_ptr(x), _dtype_code(x), rows, cols, elem_dtype, _ptr(codes),
                                           _ptr(scales), _ptr(dequant), _stream(stream)))
 

@@ -135,3 +135,67 @@ def test_generator_is_deterministic_and_reproducible_by_index():
     idx = np.array([0, 17, 4999])
     np.testing.assert_array_equal(synth.fill_at(r, synth.F16, idx), a[idx])
     np.testing.assert_array_equal(synth.fill(r, synth.F16, 10, start=17), a[17:27])
+
+
+# ---- the Python binding checks tensors before their pointers cross the ABI ----------
+
+
+def test_binding_rejects_host_tensors_before_any_launch():
+    import torch
+
+    import mixed_precision_numerics_gb300 as M
+
+    x = torch.zeros(64, dtype=torch.bfloat16)
+    y = torch.zeros(64, dtype=torch.uint8)
+    n0 = M.mp_launch_count()
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.fp8_cast_delayed(x, y, M.MP_E4M3, torch.zeros(32, dtype=torch.uint8), torch.zeros(4))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.mx_quantize(x.view(2, 32), y, torch.zeros(2, dtype=torch.uint8), M.MP_E4M3)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.fp8_quantize_blockwise(x.view(1, 64), y, torch.zeros(1), 1, 128)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.nvfp4_quantize(x.view(4, 16), y, y, torch.zeros(1), torch.zeros(1, dtype=torch.int32),
+                         torch.zeros(256, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.rht16(x.view(4, 16), torch.zeros(64), 0x5A5A)
+    w = torch.zeros(8)
+    g = torch.zeros(8, dtype=torch.float16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        M.mp_adamw_step([M.Param(w, w, w, g, g)], M.AdamwHparams(1e-3, 0.9, 0.999, 1e-8, 0.0),
+                        torch.zeros(88, dtype=torch.uint8))
+    assert M.mp_launch_count() == n0
+
+
+def test_binding_size_rule_follows_the_alignment_rule():
+    """The size check steps aside where the library itself rejects the pointer
+    (misaligned), and applies to an aligned pointer."""
+    import mixed_precision_numerics_gb300 as M
+
+    class FakeCuda:
+        is_cuda = True
+
+        def __init__(self, nbytes, ptr, device):
+            self._n, self._p, self.device = nbytes, ptr, device
+
+        def is_contiguous(self):
+            return True
+
+        def numel(self):
+            return self._n
+
+        def element_size(self):
+            return 1
+
+        def data_ptr(self):
+            return self._p
+
+    import torch
+
+    dev = torch.device("cuda", 0)
+    ref = FakeCuda(64, 4096, dev)
+    M._dev(FakeCuda(10, 4096 + 3, dev), "y", 64, like=ref)  # misaligned: left to the library
+    with pytest.raises(ValueError, match="bytes, the call needs 64"):
+        M._dev(FakeCuda(10, 4096, dev), "y", 64, like=ref)
+    with pytest.raises(ValueError, match="the call runs on"):
+        M._dev(FakeCuda(64, 4096, torch.device("cuda", 1)), "y", 64, like=ref)
