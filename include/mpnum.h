@@ -250,8 +250,10 @@ MP_API mp_status fp8_cast_delayed_count(const void* x, mp_dtype x_dtype, int64_t
  * also writes y_t [cols, rows] = transpose(y) from the same single read: the
  * backward GEMMs use the transposed operand ([NVFP4] §2.2 item 3 on the
  * transposed tensors of the backward pass).  Same scaling, amax and history
- * semantics; rows % 16 == 0 and cols % 16 == 0; x, y, y_t 16-byte aligned.
- * One kernel launch. */
+ * semantics; rows % 16 == 0 and cols % 16 == 0, rows and cols < 2^31 (else
+ * MP_ESHAPE); x, y, y_t 16-byte aligned.  One kernel launch, reading x
+ * through 2-D tensor copies: MP_ECUDA if the driver's tensor-map encoder is
+ * unavailable. */
 MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
                                             void* y, void* y_t, mp_dtype fp8_dtype, mp_fp8_meta* d_meta,
                                             float* d_history, int32_t history_len, float margin,
@@ -268,10 +270,10 @@ MP_API mp_status fp8_cast_transpose_delayed(const void* x, mp_dtype x_dtype, int
  * y = saturate(RNE(fp32(x) * r)) with r = fp8_max / amax if amax is finite
  * and > 0, else r = 0 (a NaN product gives 0x7F or, for a negative input
  * element, 0xFF).  Each block is read once.
- * cols % 16 == 0 (and rows, cols < 2^31 for 128x128 blocks, else
- * MP_ESHAPE); x, y 16-byte aligned.  One kernel launch.  The 128x128 form
- * reads its blocks through 2-D tensor copies; it returns MP_ECUDA if the
- * driver's tensor-map encoder is unavailable. */
+ * cols % 16 == 0 and rows, cols < 2^31 (else MP_ESHAPE); x, y 16-byte
+ * aligned.  One kernel launch; both block shapes read x through 2-D tensor
+ * copies of 128 x 128 boxes: MP_ECUDA if the driver's tensor-map encoder is
+ * unavailable. */
 MP_API mp_status fp8_quantize_blockwise(const void* x, mp_dtype x_dtype, int64_t rows, int64_t cols,
                                         int32_t block_rows, int32_t block_cols, void* y, mp_dtype fp8_dtype,
                                         float* scales, void* stream);
