@@ -109,16 +109,17 @@ __device__ __forceinline__ uint32_t hist_key(float h) {
 
 // At the start of a history-max cast every CTA folds a strided slice of the
 // history entries this call does not overwrite (entries blockIdx.x + k *
-// gridDim.x) into meta->internal_hrest with atomicMax: a few loads per CTA, no
-// barrier, so no CTA starts its stream late.  The last CTA reads and clears it.
+// gridDim.x) into meta->internal_hrest: the keys of a warp are reduced in
+// registers and its lane 0 issues one atomicMax, so no barrier and few
+// atomics; the last CTA reads and clears the word.  Called by whole warps.
 __device__ __forceinline__ void fold_history_slice(mp_fp8_meta* meta, const float* hist, int32_t hist_len,
                                                    int32_t slot) {
+  uint32_t k = 0;
   for (int64_t i = blockIdx.x + (int64_t)threadIdx.x * gridDim.x; i < hist_len;
-       i += (int64_t)blockDim.x * gridDim.x) {
-    if (i == slot) continue;
-    const uint32_t k = hist_key(hist[i]);
-    if (k) atomicMax(&meta->internal_hrest, k);
-  }
+       i += (int64_t)blockDim.x * gridDim.x)
+    if (i != slot) k = max(k, hist_key(hist[i]));
+  k = __reduce_max_sync(0xFFFFFFFFu, k);
+  if ((threadIdx.x & 31) == 0 && k) atomicMax(&meta->internal_hrest, k);
 }
 
 // End of every CTA: fold its amax into the meta word; the last CTA (atomic
@@ -219,7 +220,21 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
   __shared__ uint32_t red[32];
   const float scale = meta->scale;
   const int32_t slot = ((meta->pos % hist_len) + hist_len) % hist_len;  // slot taken modulo the ring length
-  if (algo == 0) fold_history_slice(meta, hist, hist_len, slot);
+  // This thread's share of the history fold (fold_history_slice's entries):
+  // the first entry is loaded now and folded after the stream, by when it has
+  // arrived, so no thread waits on it before issuing its input loads.  Entries beyond the first (only when the ring has more
+  // entries than the grid has threads) are read at the fold.
+  const int64_t h0 = blockIdx.x + (int64_t)threadIdx.x * gridDim.x;
+  const float hv = (algo == 0 && h0 < hist_len && h0 != slot) ? hist[h0] : 0.0f;
+  bool folded = algo != 0;
+  auto fold = [&]() {  // called by whole warps: one atomic per warp
+    uint32_t k = hist_key(hv);
+    for (int64_t i = h0 + (int64_t)blockDim.x * gridDim.x; i < hist_len; i += (int64_t)blockDim.x * gridDim.x)
+      if (i != slot) k = max(k, hist_key(hist[i]));
+    k = __reduce_max_sync(0xFFFFFFFFu, k);
+    if ((threadIdx.x & 31) == 0 && k) atomicMax(&meta->internal_hrest, k);
+    folded = true;
+  };
 
   float acc = 0.0f;
   uint32_t sat = 0;  // saturated elements (COUNT only)
@@ -241,6 +256,7 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
       acc = max_abs_nan(acc, vmax);
     }
   }
+  if (!folded) fold();
   // Tail elements (n % 16) go to the first CTA.
   if (blockIdx.x == 0) {
     const int64_t i = nvec * kElems + threadIdx.x;
