@@ -503,11 +503,9 @@ mp_status launch_group(const mp_param* const* list, int count, bool finalize, bo
     }
   } else {
     fill_table(Tl, list, count, kChunk);
-    static const int occ = [] {
-      cudaFuncSetAttribute(k_adamw_update<CAP, GBF16, WBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kUpdateSmem);
-      return occupancy(k_adamw_update<CAP, GBF16, WBF16>, kUpdateThreads, kUpdateSmem);
-    }();
+    static std::atomic<uint64_t> smem_done{0};
+    if (!smem_opt_in(k_adamw_update<CAP, GBF16, WBF16>, kUpdateSmem, smem_done)) return MP_ECUDA;
+    static const int occ = occupancy(k_adamw_update<CAP, GBF16, WBF16>, kUpdateThreads, kUpdateSmem);
     k_adamw_update<CAP, GBF16, WBF16><<<grid_for(Tl.tile_start[count], occ), kUpdateThreads, kUpdateSmem, s>>>(
         Tl, st, hp.beta1, hp.beta2, hp.eps);
   }

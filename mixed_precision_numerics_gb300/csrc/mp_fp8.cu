@@ -803,9 +803,8 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
   CUtensorMap map;
   memset(&map, 0, sizeof(map));  // an empty tensor still runs one CTA (the history is updated); no copy is issued
   if (rows > 0 && cols > 0 && !encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
-  static const cudaError_t attr = cudaFuncSetAttribute(
-      k_fp8_cast_t_tma<XT, E5M2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
-  if (attr != cudaSuccess) return MP_ECUDA;
+  static std::atomic<uint64_t> smem_done{0};
+  if (!smem_opt_in(k_fp8_cast_t_tma<XT, E5M2>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
   const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
   k_fp8_cast_t_tma<XT, E5M2><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, y_t, meta,
                                                                                  hist, len, margin, algo);
@@ -821,14 +820,12 @@ mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool squar
   if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
   const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
   if (square) {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_fp8_block_tma<XT, E5M2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
-    if (attr != cudaSuccess) return MP_ECUDA;
+    static std::atomic<uint64_t> smem_done{0};
+    if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, false>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     k_fp8_block_tma<XT, E5M2, false><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
   } else {
-    static const cudaError_t attr = cudaFuncSetAttribute(
-        k_fp8_block_tma<XT, E5M2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Gm::kSmem);
-    if (attr != cudaSuccess) return MP_ECUDA;
+    static std::atomic<uint64_t> smem_done{0};
+    if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, true>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     k_fp8_block_tma<XT, E5M2, true><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
   }
   note_launches(1);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/mpnum.h"
 
 namespace mp {
@@ -33,6 +35,21 @@ bool encode_tile_map_2d(CUtensorMap* map, const void* base, int esize, int64_t r
 
 // Bounded waits that gave up in this library's kernels since it was loaded.
 uint32_t fp8_wait_failures();
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on the current
+// device the first time it launches there: the attribute belongs to the
+// device, so a process driving several GPUs needs it once on each.  `done` is
+// the call site's record, one bit per device (0..63; others set it every call).
+template <typename K>
+bool smem_opt_in(K kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess) return false;
+  if (bit) done.fetch_or(bit, std::memory_order_release);
+  return true;
+}
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
