@@ -35,7 +35,8 @@ def grads(step):
 
 
 class Step:
-    """All state of one replica: optimizer, FP8 cast, NVFP4 and MX outputs."""
+    """All state of one replica: optimizer, FP8 casts (delayed, transposed,
+    blockwise), NVFP4 and MX outputs."""
 
     def __init__(self, clip: bool):
         self.params = []
@@ -58,6 +59,13 @@ class Step:
         self.nws = M.new_nvfp4_workspace()
         self.mxc = torch.zeros(256 * 256, dtype=torch.uint8, device="cuda")
         self.mxs = torch.zeros((256, 16), dtype=torch.uint8, device="cuda")
+        # the tile casts read x through 2-D tensor copies (their tensor maps
+        # travel as kernel parameters, so the graph holds them by value)
+        self.yT, self.yTt = (torch.zeros(256 * 512, dtype=torch.uint8, device="cuda") for _ in range(2))
+        self.metaT, self.histT = M.new_fp8_meta(), torch.zeros(3, device="cuda")
+        self.yb1, self.yb2 = (torch.zeros(256 * 512, dtype=torch.uint8, device="cuda") for _ in range(2))
+        self.sb1 = torch.zeros((256, 4), dtype=torch.float32, device="cuda")
+        self.sb2 = torch.zeros((2, 4), dtype=torch.float32, device="cuda")
 
     def load_inputs(self, step):
         for p, g in zip(self.params, grads(step)):
@@ -72,10 +80,15 @@ class Step:
         M.nvfp4_quantize(self.x, self.codes, self.sc, self.ts, self.nf, self.nws, stochastic=True, seed=99,
                          apply_rht=True, sign_mask=0xE3BF)
         M.mx_quantize(self.x, self.mxc, self.mxs, M.MP_E2M1)
+        M.fp8_cast_transpose_delayed(self.x, self.yT, self.yTt, M.MP_E5M2, self.metaT, self.histT, 2.0)
+        M.fp8_quantize_blockwise(self.x, self.yb1, self.sb1, 1, 128)
+        M.fp8_quantize_blockwise(self.x, self.yb2, self.sb2, 128, 128)
 
     def snapshot(self):
         out = [self.st.clone(), self.meta.clone(), self.hist.clone(), self.y8.clone(), self.codes.clone(),
-               self.sc.clone(), self.ts.clone(), self.mxc.clone(), self.mxs.clone()]
+               self.sc.clone(), self.ts.clone(), self.mxc.clone(), self.mxs.clone(), self.yT.clone(),
+               self.yTt.clone(), self.metaT.clone(), self.histT.clone(), self.yb1.clone(), self.yb2.clone(),
+               self.sb1.clone(), self.sb2.clone()]
         for p in self.params:
             out += [p.master.clone(), p.exp_avg.clone(), p.exp_avg_sq.clone(), p.working.clone()]
         return [t.view(torch.uint8) if t.dtype != torch.uint8 else t for t in out]
