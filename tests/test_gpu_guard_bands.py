@@ -38,6 +38,11 @@ def bf16(rows, cols, seed):
     return torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda().reshape(rows, cols)
 
 
+def typed(rows, cols, seed, dtype):
+    """The bf16 input widened exactly to FP32, or rounded to FP16 (values in range)."""
+    return bf16(rows, cols, seed).to(dtype)
+
+
 @pytest.mark.parametrize("n", [1, 15, 16, 4097, 100_003])
 def test_optimizer_outputs(n):
     w, m, v = (Guarded((n,), torch.float32) for _ in range(3))
@@ -59,21 +64,23 @@ def test_fp8_cast(n):
     y.check("y")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("rows,cols", [(16, 16), (48, 1040), (272, 400)])
-def test_fp8_cast_transpose(rows, cols):
+def test_fp8_cast_transpose(rows, cols, dtype):
     y, yt = Guarded((rows * cols,), torch.uint8), Guarded((rows * cols,), torch.uint8)
-    M.fp8_cast_transpose_delayed(bf16(rows, cols, 2), y.t, yt.t, M.MP_E5M2, M.new_fp8_meta(),
+    M.fp8_cast_transpose_delayed(typed(rows, cols, 2, dtype), y.t, yt.t, M.MP_E5M2, M.new_fp8_meta(),
                                  torch.zeros(4, device="cuda"))
     y.check("y")
     yt.check("y_t")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
 @pytest.mark.parametrize("br", [1, 128])
-@pytest.mark.parametrize("rows,cols", [(3, 144), (130, 272)])
-def test_fp8_blockwise(br, rows, cols):
+@pytest.mark.parametrize("rows,cols", [(3, 144), (130, 272), (1000, 1040)])
+def test_fp8_blockwise(br, rows, cols, dtype):
     y = Guarded((rows, cols), torch.uint8)
     sc = Guarded((-(-rows // br), -(-cols // 128)), torch.float32)
-    M.fp8_quantize_blockwise(bf16(rows, cols, 3), y.t, sc.t, br, 128)
+    M.fp8_quantize_blockwise(typed(rows, cols, 3, dtype), y.t, sc.t, br, 128)
     y.check("y")
     sc.check("scales")
 
