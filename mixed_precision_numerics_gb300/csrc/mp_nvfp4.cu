@@ -365,6 +365,7 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
   const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
   const int lane = threadIdx.x & 31;
   const bool odd = lane & 1;
+  const uint64_t last_use = policy_evict_first();  // this pass is the last reader of x
   const uint32_t s0 = odd ? sw.w[4] : sw.w[0], s1 = odd ? sw.w[5] : sw.w[1];
   const uint32_t s2 = odd ? sw.w[6] : sw.w[2], s3 = odd ? sw.w[7] : sw.w[3];
   const int64_t ncc = (cols + 255) / 256;
@@ -388,7 +389,8 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
     }
     uint4 raw[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) raw[r] = active ? ld_plain(x + base + r * cols) : make_uint4(0u, 0u, 0u, 0u);
+    for (int r = 0; r < 16; ++r)
+      raw[r] = active ? ld_hint(x + base + r * cols, last_use) : make_uint4(0u, 0u, 0u, 0u);
     float m;
     if (!RHT) {
       uint32_t acc[4] = {0u, 0u, 0u, 0u};
@@ -474,11 +476,12 @@ void launch_amax(const uint16_t* x, int64_t ntiles, uint32_t mask, Ws* ws, float
   k_nvfp4_amax<RHT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, mask, ws, ts, nf, keep_from);
 }
 
-// First tile (32 B each) that the amax pass of a 1x16 quantisation loads
-// with the L2 evict-last policy: the last half-L2's worth of x, which the
-// encode pass then reads first (and with evict-first, releasing it).  The
-// 16x16 path reads x in the same order in both passes, so it marks nothing;
-// its weights usually fit in L2 whole.  The L2 size is read once per process.
+// First tile (32 B each) that the amax pass loads with the L2 evict-last
+// policy, so that the encode pass (which reads with evict-first, releasing the
+// lines) finds it in L2.  1x16: the last half-L2's worth of x, which the
+// encode pass reads first.  16x16: the whole tensor when it fits in half the
+// L2 (a weight matrix usually does), else nothing, since that pass reads x in
+// the same order as the amax pass.  The L2 size is read once per process.
 int64_t keep_from_of(int64_t ntiles, bool block_2d) {
   static const int64_t l2 = [] {
     int dev = 0, v = 0;
@@ -486,8 +489,8 @@ int64_t keep_from_of(int64_t ntiles, bool block_2d) {
       v = 0;
     return (int64_t)v;
   }();
-  if (block_2d) return ntiles;
   const int64_t keep = l2 / 2 / 32;
+  if (block_2d) return ntiles <= keep ? 0 : ntiles;
   return ntiles > keep ? ntiles - keep : 0;
 }
 
