@@ -21,6 +21,7 @@
 // mp_wait_failures.
 #include <string.h>
 
+#include "mp_chain.cuh"
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -216,6 +217,8 @@ __global__ __launch_bounds__(kThreads) void k_fp8_cast(const void* __restrict__ 
                                                        uint8_t* __restrict__ y, mp_fp8_meta* meta,
                                                        float* hist, int32_t hist_len, float margin, int32_t algo,
                                                        unsigned long long* saturated_out) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   constexpr int U = unroll_of<XT>();
   __shared__ uint32_t red[32];
   const float scale = meta->scale;
@@ -471,6 +474,8 @@ template <int XT, bool E5M2, bool ROWS>
 __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
     float* __restrict__ scales) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   using Gm = BlkGeom<XT>;
   constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG;  // groups per row
   constexpr int kNG = Gm::kGroups;
@@ -646,6 +651,8 @@ template <int XT, bool E5M2>
 __global__ __launch_bounds__(TrGeom<XT>::kThreads, 1) void k_fp8_cast_t_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
     uint8_t* __restrict__ y_t, mp_fp8_meta* meta, float* hist, int32_t hist_len, float margin, int32_t algo) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   using Gm = TrGeom<XT>;
   constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG, kNG = Gm::kGroups;
   constexpr int kRowStep = kGroupThreads / kGpr;
@@ -789,8 +796,8 @@ mp_status launch(const void* x, int64_t n, uint8_t* y, mp_fp8_meta* meta, float*
   const int64_t nvec = n / kElems;
   constexpr int U = unroll_of<XT>();
   const int64_t ctas = (nvec + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
-  k_fp8_cast<XT, E5M2, COUNT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, n, y, meta, hist, len, margin, algo,
-                                                                       saturated);
+  launch_chained(k_fp8_cast<XT, E5M2, COUNT>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, n, y, meta, hist, len,
+                 margin, algo, saturated);
   note_launches(1);
   return launch_status();
 }
@@ -806,8 +813,8 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
   static std::atomic<uint64_t> smem_done{0};
   if (!smem_opt_in(k_fp8_cast_t_tma<XT, E5M2>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
   const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
-  k_fp8_cast_t_tma<XT, E5M2><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, y_t, meta,
-                                                                                 hist, len, margin, algo);
+  launch_chained(k_fp8_cast_t_tma<XT, E5M2>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map, rows, cols,
+                 y, y_t, meta, hist, len, margin, algo);
   note_launches(1);
   return launch_status();
 }
@@ -822,11 +829,13 @@ mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool squar
   if (square) {
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, false>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
-    k_fp8_block_tma<XT, E5M2, false><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
+    launch_chained(k_fp8_block_tma<XT, E5M2, false>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
+                   rows, cols, y, scales);
   } else {
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, true>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
-    k_fp8_block_tma<XT, E5M2, true><<<grid_for(boxes, 1), Gm::kThreads, Gm::kSmem, s>>>(map, rows, cols, y, scales);
+    launch_chained(k_fp8_block_tma<XT, E5M2, true>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
+                   rows, cols, y, scales);
   }
   note_launches(1);
   return launch_status();

@@ -14,6 +14,7 @@
 // the warp reads one contiguous 2 KB (4 KB) span, writes one contiguous run of
 // codes and a 32-byte run of scale bytes.  Two blocks (one for FP32) are in
 // flight per thread: 128 B of loads.
+#include "mp_chain.cuh"
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -162,6 +163,8 @@ template <int XT, int EF>
 __global__ __launch_bounds__(kThreads) void k_mx_quantize(const void* __restrict__ x, int64_t nblk,
                                                           uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                           uint16_t* __restrict__ dq) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   constexpr int U = unroll_of<XT>(), W = words_of<XT>();
   const uint4* xv = static_cast<const uint4*>(x);
   for (int64_t base = (int64_t)blockIdx.x * kThreads * U; base < nblk; base += (int64_t)gridDim.x * kThreads * U) {
@@ -194,7 +197,7 @@ mp_status launch(const void* x, int64_t nblk, uint8_t* codes, uint8_t* scales, u
   static const int occ = occ_of(k_mx_quantize<XT, EF>);
   constexpr int U = unroll_of<XT>();
   const int64_t ctas = (nblk + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
-  k_mx_quantize<XT, EF><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, nblk, codes, scales, dq);
+  launch_chained(k_mx_quantize<XT, EF>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, nblk, codes, scales, dq);
   note_launches(1);
   return launch_status();
 }

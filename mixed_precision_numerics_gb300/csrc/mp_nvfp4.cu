@@ -22,6 +22,7 @@
 // that its additions happen in the documented order.
 #include <mutex>
 
+#include "mp_chain.cuh"
 #include "mp_device.cuh"
 #include "mp_internal.h"
 
@@ -90,6 +91,8 @@ template <bool RHT>
 __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restrict__ x, int64_t ntiles,
                                                          uint32_t mask, Ws* ws, float* tensor_scale,
                                                          int32_t* nonfinite, int64_t keep_from) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   __shared__ uint32_t red[32];
   __shared__ int is_last;
   const SignWords sw = sign_words(mask);
@@ -245,6 +248,8 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
                                                          const int32_t* __restrict__ nonfinite,
                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                          uint16_t* __restrict__ deq) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   const float s_t = *tensor_scale;
   const bool zero = (*nonfinite != 0) || s_t == 0.0f;
   const SignWords sw = sign_words(mask);
@@ -359,6 +364,8 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
                                                        const int32_t* __restrict__ nonfinite,
                                                        uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                        uint16_t* __restrict__ deq) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   const float s_t = *tensor_scale;
   const bool zero = (*nonfinite != 0) || s_t == 0.0f;
   const SignWords sw = sign_words(mask);
@@ -440,6 +447,8 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
 template <bool F32OUT>
 __global__ __launch_bounds__(kThreads) void k_rht16(const uint16_t* __restrict__ x, int64_t ntiles, uint32_t mask,
                                                     void* __restrict__ y) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
   const SignWords sw = sign_words(mask);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   for (int64_t t = (int64_t)blockIdx.x * kThreads + threadIdx.x; t < ntiles; t += stride) {
@@ -473,7 +482,8 @@ void launch_amax(const uint16_t* x, int64_t ntiles, uint32_t mask, Ws* ws, float
                  cudaStream_t s) {
   static const int occ = occ_of(k_nvfp4_amax<RHT>);
   const int64_t ctas = (ntiles + 2 * kThreads - 1) / (2 * kThreads);
-  k_nvfp4_amax<RHT><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, mask, ws, ts, nf, keep_from);
+  launch_chained(k_nvfp4_amax<RHT>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, ntiles, mask, ws, ts, nf,
+                 keep_from);
 }
 
 // First tile (32 B each) that the amax pass loads with the L2 evict-last
@@ -502,14 +512,14 @@ void launch_encode(bool block_2d, const uint16_t* x, int64_t rows, int64_t cols,
     static const int occ = occ_of(k_nvfp4_2d<RHT, SR, DEQ>);
     const int64_t items = (rows / 16) * ((cols + 255) / 256);  // one warp each
     const int64_t ctas = (items + kThreads / 32 - 1) / (kThreads / 32);
-    k_nvfp4_2d<RHT, SR, DEQ><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, rows, cols, mask, seed, ts, nf, codes,
-                                                                       scales, deq);
+    launch_chained(k_nvfp4_2d<RHT, SR, DEQ>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, rows, cols, mask, seed,
+                   ts, nf, codes, scales, deq);
   } else {
     static const int occ = occ_of(k_nvfp4_1x16<RHT, SR, DEQ>);
     const int64_t nblocks = rows * (cols / 16);
     const int64_t ctas = (nblocks + kThreads - 1) / kThreads;
-    k_nvfp4_1x16<RHT, SR, DEQ><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, nblocks, mask, seed, ts, nf, codes,
-                                                                         scales, deq);
+    launch_chained(k_nvfp4_1x16<RHT, SR, DEQ>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, nblocks, mask, seed,
+                   ts, nf, codes, scales, deq);
   }
 }
 
@@ -580,10 +590,10 @@ MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t 
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   if (y_dtype == MP_F32) {
     static const int occ = occ_of(k_rht16<true>);
-    k_rht16<true><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, sign_mask, y);
+    launch_chained(k_rht16<true>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
   } else {
     static const int occ = occ_of(k_rht16<false>);
-    k_rht16<false><<<grid_for(ctas, occ), kThreads, 0, s>>>(x, ntiles, sign_mask, y);
+    launch_chained(k_rht16<false>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
   }
   note_launches(1);
   return launch_status();
