@@ -31,6 +31,11 @@
  *     be anything >= 0 unless stated.
  *   - Calls that share a state struct, meta struct or workspace must be
  *     ordered on one stream; calls with disjoint state may run concurrently.
+ *   - The quantiser kernels (FP8, NVFP4, MX, the transform) are launched with
+ *     programmatic stream serialization allowed: their blocks may be
+ *     scheduled while the previous kernel in the stream finishes, but each
+ *     waits for that kernel to complete (griddepcontrol.wait) before touching
+ *     memory, so the stream order seen by memory is unchanged.
  */
 #ifndef MPNUM_H
 #define MPNUM_H
