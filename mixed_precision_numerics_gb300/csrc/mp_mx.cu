@@ -86,9 +86,9 @@ __device__ __forceinline__ uint32_t encode_pair(float a, float b) {
   } else if constexpr (EF == EE3M2) {
     return cvt_e3m2x2(a, b);
   } else {
-    constexpr float fmax = EF == EE5M2 ? 57344.0f : 448.0f;
-    a = fminf(fmaxf(a, -fmax), fmax);
-    b = fminf(fmaxf(b, -fmax), fmax);
+    // The block is finite and scaled so its maximum is below twice the
+    // format's largest value: the conversion's satfinite mode takes anything
+    // beyond that largest value to it, as a clamp would.
     return EF == EE5M2 ? cvt_e5m2x2(a, b) : cvt_e4m3x2(a, b);
   }
 }
@@ -119,10 +119,10 @@ __device__ __forceinline__ void mx_block(const uint4* raw, int64_t blk, uint8_t*
     const uint32_t p = bad ? 0u : encode_pair<EF>(__fmul_rn(f.x, mul), __fmul_rn(f.y, mul));
     if constexpr (EF == EE2M1) {
       if ((k & 3) == 0) w[k >> 2] = 0u;
-      w[k >> 2] |= p << (8 * (k & 3));
+      w[k >> 2] += p << (8 * (k & 3));  // disjoint fields: + is |
     } else {
       if ((k & 1) == 0) w[k >> 1] = 0u;
-      w[k >> 1] |= p << (16 * (k & 1));
+      w[k >> 1] += p << (16 * (k & 1));
     }
   }
   if constexpr (EF == EE2M1) {
