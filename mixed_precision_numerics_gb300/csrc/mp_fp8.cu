@@ -314,8 +314,10 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
 // elements) of the stage into registers and releases the stage at once, so
 // the next copy starts while the block is reduced (four independent maxima,
-// warp shuffles, then one named barrier per group, the partial maxima
-// double-buffered by round) and cast from registers.  Warp w of a group takes
+// packed for 16-bit input, a warp reduction, then one named barrier per
+// group, the partial maxima double-buffered by round; the 1x128 form instead
+// takes each row's maximum by a recursive-halving shuffle exchange and needs
+// no barrier) and cast from registers.  Warp w of a group takes
 // rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15), whole rows,
 // so shared-memory reads cover 512 consecutive bytes per instruction and
 // every store writes whole row segments.  Parts of an edge block outside the
