@@ -17,9 +17,12 @@
 //                   per block.
 // For 1x16 the amax pass loads the last half-L2's worth of x with the L2
 // evict-last policy and the encode pass walks x from the end, so that part
-// of the second read is served by L2.
-// The transform is evaluated on CUDA cores by the butterfly in binary32 so
-// that its additions happen in the documented order.
+// of the second read is served by L2; a 16x16 input that fits in half the L2
+// is kept whole.  The 16x16 encode gives each warp a 16-row strip (a block is
+// a lane pair), with no CTA barrier.  The transform is evaluated on CUDA
+// cores by the butterfly in binary32, three of its stages as packed FP32x2
+// operations, so that its additions happen in the documented order.  Both
+// passes are chained launches (mp_chain.cuh).
 #include <mutex>
 
 #include "mp_chain.cuh"
