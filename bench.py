@@ -24,7 +24,6 @@ import argparse
 import ctypes
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -456,42 +455,28 @@ class Workload:
         return out
 
     # ---- end to end through host buffers -------------------------------------------------
-    def pinned_block(self, specs):
-        """One pinned host allocation carved into tensors of the given
-        (shape, dtype), each 256-byte aligned: one host registration for all
-        of a step's inputs (or results) instead of one per tensor."""
-        torch = self.torch
-        offs, o = [], 0
-        for shape, dt in specs:
-            nb = math.prod(shape) * torch.empty(0, dtype=dt).element_size()
-            offs.append((o, nb))
-            o += (nb + 255) // 256 * 256
-        blk = torch.empty(max(o, 256), dtype=torch.uint8, pin_memory=True)
-        return blk, [blk[a:a + nb].view(dt).view(shape) for (shape, dt), (a, nb) in zip(specs, offs)]
-
     def e2e_setup(self):
         """Pinned host copies of every input, pinned host buffers for the
         results, and a second device input set so that a step's inputs can be
-        copied in while the previous step runs."""
+        copied in while the previous step runs.  One pinned buffer per tensor:
+        the host allocator rounds each allocation up to a power of two, which
+        costs less per tensor (about 20 GB for the step's 16.6 GB) than for one
+        block holding them all (32 GB); the copy rate is the same either way."""
         torch, M = self.torch, self.M
 
-        srcs = [t.grad for t in self.tensors] + list(self.act[:2]) + list(self.grd[:2]) + [q["x"] for q in self.q]
-        self.h_in_block, h_in = self.pinned_block([(tuple(d.shape), d.dtype) for d in srcs])
-        for h, d in zip(h_in, srcs):
+        def pinned_copy(d):
+            h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
             h.copy_(d)
-        nt = len(self.tensors)
-        self.h_grads = h_in[:nt]
-        self.h_act = h_in[nt:nt + 2]
-        self.h_grd = h_in[nt + 2:nt + 4]
-        self.h_q = h_in[nt + 4:]
-        outs = [((self.fp8_n,), torch.uint8)] * 2
-        for q in self.q:
-            outs += [(tuple(q["codes"].shape), torch.uint8), (tuple(q["scales"].shape), torch.uint8)]
-        outs.append(((88 + 64 + 3 * 8,), torch.uint8))
-        self.h_out_block, h_out = self.pinned_block(outs)
-        self.h_out_fp8 = h_out[:2]
-        self.h_out_q = [(h_out[2 + 2 * i], h_out[3 + 2 * i]) for i in range(len(self.q))]
-        self.h_small = h_out[-1]
+            return h
+
+        self.h_grads = [pinned_copy(t.grad) for t in self.tensors]
+        self.h_act = [pinned_copy(a) for a in self.act[:2]]
+        self.h_grd = [pinned_copy(g) for g in self.grd[:2]]
+        self.h_q = [pinned_copy(q["x"]) for q in self.q]
+        self.h_out_fp8 = [torch.empty(self.fp8_n, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+        self.h_out_q = [(torch.empty(q["codes"].shape, dtype=torch.uint8, pin_memory=True),
+                         torch.empty(q["scales"].shape, dtype=torch.uint8, pin_memory=True)) for q in self.q]
+        self.h_small = torch.empty(88 + 64 + 3 * 8, dtype=torch.uint8, pin_memory=True)
         self.h2d = sum(h.numel() * h.element_size() for h in self.h_grads) + 2 * self.fp8_n * 2 + \
             sum(h.numel() * h.element_size() for h in self.h_q)
         self.d2h = 2 * self.fp8_n + sum(c.numel() + s.numel() for c, s in self.h_out_q) + 88 + 64 + 24
