@@ -206,3 +206,19 @@ def test_full_size_gradients_rht_sr():
     dq = O.convert(got[4][:512], O.BF16, O.F32).astype(np.float64)
     err = (dq - xp).ravel()
     assert abs(err.mean()) < 5 * err.std() / np.sqrt(err.size)
+
+
+def test_random_shape_sweep_2d_against_the_oracle():
+    """Seeded random 16x16-block shapes (rows and cols multiples of 16, from one
+    partial 16 x 256 strip to several strips per warp) with the transform and
+    stochastic rounding on and off: codes, scales, tensor scale and dequantised
+    values match the oracle bit for bit."""
+    rng = np.random.default_rng(2027)
+    for i in range(12):
+        rows = 16 * int(rng.integers(1, 40))
+        cols = 16 * int(rng.integers(1, 130))
+        sr, rht = bool(i & 1), bool(i & 2)
+        x = mixed_input(rows, cols, 500 + i)
+        got = gpu_quant(x, True, sr, 77 + i, rht, 0x5A3C)
+        ref = O.nvfp4_quantize(x, True, sr, 77 + i, rht, 0x5A3C)
+        assert_same(got, ref, f"{rows}x{cols} sr={sr} rht={rht}")
