@@ -338,3 +338,35 @@ def test_saturation_count_matches_the_oracle(fmt, dtype):
         assert torch.equal(h1.view(torch.int32), h2.view(torch.int32))  # bits: the amax may be NaN
         total += O.fp8_saturation_count(x, XFMT[dtype], FMT[fmt], scale)
         assert int(sat.item()) == total
+
+
+def test_chained_launches_see_the_previous_kernels_writes():
+    """The quantisers are launched with programmatic stream serialization; each
+    waits for the previous kernel before touching memory.  A torch kernel that
+    rewrites the input right before every call must be seen by that call, and
+    each FP8 cast must see the scale its predecessor left in the meta, with no
+    synchronisation anywhere in the loop."""
+    n = 1 << 20
+    steps = 40
+    x = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+    ys = torch.empty((steps, n), dtype=torch.uint8, device="cuda")
+    codes = torch.empty((steps, n // 2), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((steps, n // 16), dtype=torch.uint8, device="cuda")
+    ts = torch.empty(steps, dtype=torch.float32, device="cuda")
+    nf = torch.empty(steps, dtype=torch.int32, device="cuda")
+    ws = M.new_nvfp4_workspace()
+    meta, hist = M.new_fp8_meta(), torch.zeros(4, device="cuda")
+    vals = [float(2.0 ** (k % 7 - 3)) * (1 + (k % 3) / 8) for k in range(steps)]
+    for k, v in enumerate(vals):
+        x.fill_(v)  # a torch kernel writes the input
+        M.fp8_cast_delayed(x, ys[k], M.MP_E4M3, meta, hist)
+        M.nvfp4_quantize(x.view(1024, 1024), codes[k], sc[k], ts[k:k + 1], nf[k:k + 1], ws)
+    torch.cuda.synchronize()
+    om, oh = O.new_fp8_meta(), np.zeros(4, np.float32)
+    for k, v in enumerate(vals):
+        xb = O.convert(np.full(16, v, np.float32), O.F32, O.BF16)  # the same constant tensor, 16 elements
+        want = O.fp8_cast_delayed(xb, O.BF16, O.E4M3, om, oh, 1.0)[0]
+        assert bool((ys[k] == int(want)).all()), f"iteration {k}: the FP8 cast saw a stale input or scale"
+        xv = (xb[:1].astype(np.uint32) << 16).view(np.float32)[0]
+        assert np.float32(ts[k].item()) == np.float32(xv) / np.float32(2688.0), f"iteration {k}: tensor scale"
+    assert_meta_equal(M.read_fp8_meta(meta), om)
