@@ -112,8 +112,7 @@ def lib() -> ctypes.CDLL:
             "orc_adamw_begin": (None, [P, P, ctypes.c_int, P]),
             "orc_adamw_apply": (None, [P, P, P, P, P, ctypes.c_int, P, ctypes.c_int, I64]),
             "orc_loss_scale_update": (None, [P, P]),
-            "orc_grad_tile_sums": (None, [P, ctypes.c_int, I64, F, P]),
-            "orc_sum_tile_sums": (ctypes.c_double, [P, I64]),
+            "orc_grad_sumsq": (ctypes.c_double, [P, ctypes.c_int, I64, F]),
             "orc_clip_coef": (F, [ctypes.c_double, F]),
             "orc_fp8_cast_one": (U8, [F, F, ctypes.c_int]),
             "orc_fp8_cast_array": (None, [P, ctypes.c_int, I64, P, ctypes.c_int, F]),
@@ -387,19 +386,10 @@ def nvfp4_block_scale(bamax: float, s_t: float):
     return int(c[0]), float(d[0]), float(r[0])
 
 
-CLIP_TILE = 16384
-
-
-def grad_tile_sums(g: np.ndarray, g_fmt: int, inv_scale: float) -> np.ndarray:
+def grad_sumsq(g: np.ndarray, g_fmt: int, inv_scale: float) -> float:
+    """Sum of squares of one tensor's unscaled grads, binary64, element order."""
     g = np.ascontiguousarray(g, dtype=np.uint16)
-    out = np.zeros((g.size + CLIP_TILE - 1) // CLIP_TILE, dtype=np.float32)
-    lib().orc_grad_tile_sums(_p(g), g_fmt, g.size, np.float32(inv_scale), _p(out))
-    return out
-
-
-def sum_tile_sums(tiles: np.ndarray) -> float:
-    tiles = np.ascontiguousarray(tiles, dtype=np.float32)
-    return float(lib().orc_sum_tile_sums(_p(tiles), tiles.size))
+    return float(lib().orc_grad_sumsq(_p(g), g_fmt, g.size, np.float32(inv_scale)))
 
 
 def clip_coef(norm: float, max_norm: float) -> float:
@@ -407,19 +397,27 @@ def clip_coef(norm: float, max_norm: float) -> float:
 
 
 def grad_norm(grads, g_fmt: int, inv_scale: float) -> float:
-    """Global L2 norm of the unscaled grads, in the fixed order of oracle.h."""
-    tiles = [grad_tile_sums(g, g_fmt, inv_scale) for g in grads if g.size]
-    total = sum_tile_sums(np.concatenate(tiles) if tiles else np.zeros(0, np.float32))
+    """Global L2 norm of the unscaled grads: the tensors' binary64 sums of
+    squares added in list order, then the square root."""
+    return norm_of_sumsqs([grad_sumsq(g, g_fmt, inv_scale) for g in grads])
+
+
+def norm_of_sumsqs(sums) -> float:
+    total = 0.0
+    for x in sums:
+        total = total + x
     return float(np.sqrt(total))
 
 
-def adamw_step(hp: AdamwHp, st: ScalerState, tensors, g_fmt: int, w16_fmt: int):
+def adamw_step(hp: AdamwHp, st: ScalerState, tensors, g_fmt: int, w16_fmt: int, clip=None):
     """One optimizer step over a list of (w, m, v, g, w16) numpy tensors.
 
     found_inf is the OR over every grad of the step; when set the step is
     skipped and nothing is written.  With hp.max_grad_norm > 0 the unscaled
-    grads are clipped to that global norm.  Returns (found_inf, grad norm or
-    None, clip coefficient)."""
+    grads are clipped to that global norm.  ``clip``, when given, is the
+    binary32 clip coefficient to multiply by in place of the one formed from
+    this norm (a test applies a coefficient it has checked separately).
+    Returns (found_inf, grad norm or None, clip coefficient of the norm)."""
     found = 0
     for (_, _, _, g, _) in tensors:
         if nonfinite_any(g, g_fmt):
@@ -430,7 +428,10 @@ def adamw_step(hp: AdamwHp, st: ScalerState, tensors, g_fmt: int, w16_fmt: int):
     if hp.max_grad_norm > 0:
         norm = grad_norm([g for (_, _, _, g, _) in tensors], g_fmt, s.inv_scale)
         s.clip = clip_coef(norm, hp.max_grad_norm)
+    coef = s.clip
+    if clip is not None:
+        s.clip = float(np.float32(clip))
     if not found:
         for (w, m, v, g, w16) in tensors:
             adamw_apply(s, w, m, v, g, g_fmt, w16, w16_fmt)
-    return found, norm, s.clip
+    return found, norm, coef

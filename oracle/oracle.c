@@ -371,59 +371,22 @@ void orc_adamw_apply(const orc_step_scalars* s, float* w, float* m, float* v, co
   }
 }
 
-/* Global gradient norm in the fixed order stated in oracle.h. */
-void orc_grad_tile_sums(const uint16_t* g, int g_fmt, int64_t n, float inv_scale, float* tile_sums) {
-  int64_t ntiles = (n + ORC_CLIP_TILE - 1) / ORC_CLIP_TILE;
-  float lane[256], grp[8];
-  for (int64_t tile = 0; tile < ntiles; ++tile) {
-    int64_t base = tile * ORC_CLIP_TILE;
-    for (int t = 0; t < 256; ++t) {
-      float s = 0.0f;
-      for (int u = 0; u < 8; ++u)
-        for (int k = 0; k < 8; ++k) {
-          int64_t i = base + u * 2048 + t * 8 + k;
-          if (i >= n) continue;
-          float gf = (g_fmt == ORC_F16) ? orc_f16_to_f32(g[i]) : orc_bf16_to_f32(g[i]);
-          float gu = gf * inv_scale;
-          s = s + gu * gu;
-        }
-      lane[t] = s;
-    }
-    for (int w = 0; w < 8; ++w) {
-      float v[32], nv[32];
-      for (int l = 0; l < 32; ++l) v[l] = lane[w * 32 + l];
-      for (int h = 16; h >= 1; h >>= 1) {
-        for (int l = 0; l < 32; ++l) nv[l] = v[l] + v[l ^ h];
-        for (int l = 0; l < 32; ++l) v[l] = nv[l];
-      }
-      grp[w] = v[0];
-    }
-    for (int h = 4; h >= 1; h >>= 1)
-      for (int i = 0; i < h; ++i) grp[i] = grp[i] + grp[i + h];
-    tile_sums[tile] = grp[0];
+/* Sum of squares of one tensor's unscaled grads, the quantity whose square
+ * root over all tensors is the L2 norm that clip_grad_norm_ compares with
+ * max_norm ([MPT-ko] "FP16 학습 루프": unscale_ then clip_grad_norm_;
+ * [MPT-es] "Operaciones que permanecen en FP32": norms are long reductions
+ * kept in high precision).  The unscaled grad is the binary32 value the update
+ * uses, gu = fp32(grad) * inv_scale; its square is exact in binary64 (24-bit
+ * significands), and the squares are added one after another in element
+ * order in binary64. */
+double orc_grad_sumsq(const uint16_t* g, int g_fmt, int64_t n, float inv_scale) {
+  double total = 0.0;
+  for (int64_t i = 0; i < n; ++i) {
+    float gf = (g_fmt == ORC_F16) ? orc_f16_to_f32(g[i]) : orc_bf16_to_f32(g[i]);
+    double gu = (double)(gf * inv_scale);
+    total = total + gu * gu;
   }
-}
-
-double orc_sum_tile_sums(const float* tile_sums, int64_t ntiles) {
-  double lane[1024];
-  double grp[32];
-  for (int t = 0; t < 1024; ++t) {
-    double s = 0.0;
-    for (int64_t i = t; i < ntiles; i += 1024) s = s + (double)tile_sums[i];
-    lane[t] = s;
-  }
-  for (int w = 0; w < 32; ++w) {
-    double v[32], nv[32];
-    for (int l = 0; l < 32; ++l) v[l] = lane[w * 32 + l];
-    for (int h = 16; h >= 1; h >>= 1) {
-      for (int l = 0; l < 32; ++l) nv[l] = v[l] + v[l ^ h];
-      for (int l = 0; l < 32; ++l) v[l] = nv[l];
-    }
-    grp[w] = v[0];
-  }
-  for (int h = 16; h >= 1; h >>= 1)
-    for (int i = 0; i < h; ++i) grp[i] = grp[i] + grp[i + h];
-  return grp[0];
+  return total;
 }
 
 float orc_clip_coef(double norm, float max_norm) {

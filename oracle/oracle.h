@@ -121,23 +121,13 @@ void orc_adamw_apply(const orc_step_scalars* s, float* w, float* m, float* v, co
                      int g_fmt, uint16_t* w16, int w16_fmt, int64_t n);
 /* Gradient-norm clipping ([MPT-ko] "FP16 학습 루프": clip_grad_norm_(max_norm=1.0)
  * after unscale_; [MPT-es] "Operaciones que permanecen en FP32": long
- * reductions such as gradient norms stay in FP32).  The sum of squares of
- * the unscaled grads g = fp32(grad) * inv_scale uses one fixed order:
- *   tiles of 16384 elements per tensor (the last one short);
- *   in a tile, lane t (0..255) sums, in binary32, g*g of the elements
- *     u*2048 + t*8 + k for u = 0..7, then k = 0..7;
- *   the 256 lane sums fold as 8 groups of 32: in each, v[l] += v[l ^ h] for
- *     h = 16, 8, 4, 2, 1, keeping v[0]; the 8 group results w fold as
- *     w[i] += w[i + h] for i < h, h = 4, 2, 1, keeping w[0];
- *   tile sums, in tile order over all tensors, fold in binary64: lane t of
- *     1024 adds tiles t, t + 1024, ... in order, then the 1024 lane sums fold
- *     as 32 groups of 32 (v[l] += v[l ^ h], h = 16..1) and the 32 group
- *     results as w[i] += w[i + h], h = 16..1.
- * norm = sqrt(total); clip = min(1, max_norm / (norm + 1e-6)), binary64,
- * rounded to binary32. */
-#define ORC_CLIP_TILE 16384
-void orc_grad_tile_sums(const uint16_t* g, int g_fmt, int64_t n, float inv_scale, float* tile_sums);
-double orc_sum_tile_sums(const float* tile_sums, int64_t ntiles);
+ * reductions such as gradient norms stay in high precision).  The norm is the
+ * L2 norm of all unscaled grads g = fp32(grad) * inv_scale (binary32, as the
+ * update uses them): orc_grad_sumsq returns one tensor's sum of g*g, squares
+ * exact in binary64 and added in element order in binary64; the caller adds
+ * the tensors' sums in list order in binary64, norm = sqrt(total).
+ * clip = min(1, max_norm / (norm + 1e-6)), binary64, rounded to binary32. */
+double orc_grad_sumsq(const uint16_t* g, int g_fmt, int64_t n, float inv_scale);
 float orc_clip_coef(double norm, float max_norm);
 /* Dynamic loss-scale update from st->found_inf. */
 void orc_loss_scale_update(orc_scaler_state* st, const orc_scaler_cfg* cfg);

@@ -1,10 +1,13 @@
 """Pins for the oracle's gradient-norm clipping (CPU).
 
-The fixed summation order is checked where the exact answer is known
-(integer-valued grads, whose squares and partial sums are exact in binary32),
-against numpy's float64 norm elsewhere, and the clipped step against the
-closed form of Adam's first update.
+The norm is the plain definition (squares of the binary32 unscaled grads,
+exact in binary64, summed in order in binary64).  It is checked where the
+exact answer is known (integer-valued grads), against math.fsum's correctly
+rounded sum and numpy's pairwise float64 norm within the binary64 summation
+bound, and the clipped step against the closed form of Adam's first update.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -24,14 +27,58 @@ def test_sum_of_squares_is_exact_for_integer_grads(sizes):
     assert norm == np.sqrt(float(exact))
 
 
-def test_norm_matches_float64_and_unscales_first():
+U64 = 2.0 ** -53
+
+
+@pytest.mark.parametrize("g_fmt", [O.F16, O.BF16])
+def test_norm_matches_fsum_and_unscales_first(g_fmt):
     rng = np.random.default_rng(5)
     S = 1024.0
-    grads = [(rng.standard_normal(n) * 1e-2 * S).astype(np.float32) for n in (5, 20000, 70001)]
-    g16 = [f16(g) for g in grads]
-    exact = np.sqrt(sum(float(((O.convert(g, O.F16, O.F32).astype(np.float64) / S) ** 2).sum()) for g in g16))
-    norm = O.grad_norm(g16, O.F16, float(np.float32(1.0 / S)))
-    assert norm == pytest.approx(exact, rel=2e-6)
+    sizes = (5, 20000, 70001)
+    grads = [(rng.standard_normal(n) * 1e-2 * S).astype(np.float32) for n in sizes]
+    g16 = [O.convert(g, O.F32, g_fmt) for g in grads]
+    # S is a power of two: the binary32 unscale is exact, so the squares of
+    # fp32(grad) / S are the exact terms; fsum rounds their sum once.
+    terms = [float(x) ** 2 for g in g16 for x in (O.convert(g, g_fmt, O.F32).astype(np.float64) / S)]
+    exact = math.fsum(terms)
+    norm = O.grad_norm(g16, g_fmt, float(np.float32(1.0 / S)))
+    n = sum(sizes)
+    # n binary64 additions of non-negative terms, then one square root
+    assert abs(norm * norm - exact) <= (n + len(sizes)) * U64 * exact * 1.01
+    assert abs(norm - math.sqrt(exact)) <= ((n + len(sizes)) * U64 / 2 + U64) * math.sqrt(exact)
+    pairwise = np.sqrt(sum(float(((O.convert(g, g_fmt, O.F32).astype(np.float64) / S) ** 2).sum()) for g in g16))
+    assert norm == pytest.approx(pairwise, rel=n * U64)
+
+
+def test_norm_squares_the_binary32_unscaled_grad():
+    # S = 3: 1/S is not a power of two, so fp32(g) * fp32(1/S) rounds; the
+    # norm of one element is the magnitude of that binary32 product, exactly.
+    inv = float(np.float32(1.0 / 3.0))
+    for v in (1.0, 7.0, -1000.0, 65504.0, 2.0 ** -24):
+        g = f16([v])
+        gu = np.float32(O.convert(g, O.F16, O.F32)[0]) * np.float32(inv)
+        assert O.grad_norm([g], O.F16, inv) == abs(float(gu))
+
+
+def test_norm_of_split_tensors_adds_their_sums():
+    rng = np.random.default_rng(11)
+    g = f16(rng.standard_normal(50000))
+    whole = O.grad_norm([g], O.F16, 1.0)
+    parts = O.grad_norm([g[:12345], g[12345:40000], g[40000:]], O.F16, 1.0)
+    assert parts == pytest.approx(whole, rel=50000 * U64)
+    assert O.grad_norm([], O.F16, 1.0) == 0.0
+    assert O.grad_norm([g[:0]], O.F16, 1.0) == 0.0
+
+
+def test_non_finite_grads_give_a_non_finite_norm():
+    g = f16([1.0, 2.0, 3.0])
+    inf = g.copy()
+    inf[1] = 0x7C00
+    nan = g.copy()
+    nan[2] = 0x7E00
+    assert O.grad_norm([g], O.F16, 1.0) == math.sqrt(14.0)
+    assert math.isinf(O.grad_norm([g, inf], O.F16, 1.0))
+    assert math.isnan(O.grad_norm([nan, g], O.F16, 1.0))
 
 
 def test_clip_coefficient_closed_form():
