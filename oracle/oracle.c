@@ -51,7 +51,7 @@ static double decode_mag(uint32_t field_e, uint32_t mant, int M, int emin, int b
 
 /* --- FP16 ([MPT-ko] "왜 그냥 FP16으로는 안 되는가"; [MPT-es] "Formatos") ---- */
 uint16_t orc_f32_to_f16(float x) {
-  if (isnan(x)) return 0x7FFF;
+  if (isnan(x)) return 0x7FFF; /* reading R-NaN16: the canonical NaN's image */
   uint16_t s = signbit(x) ? 0x8000 : 0;
   double a = fabs((double)x);
   if (isinf(x)) return s | 0x7C00;
@@ -69,7 +69,7 @@ float orc_f16_to_f32(uint16_t h) {
 
 /* --- BF16 ([MPT-es] "Formatos de coma flotante") ------------------------- */
 uint16_t orc_f32_to_bf16(float x) {
-  if (isnan(x)) return 0x7FFF;
+  if (isnan(x)) return 0x7FFF; /* reading R-NaN16: the canonical NaN's image */
   uint16_t s = signbit(x) ? 0x8000 : 0;
   if (isinf(x)) return s | 0x7F80;
   double a = fabs((double)x);

@@ -22,8 +22,9 @@
  * library routines.  Philox4x32-10 is pinned against an independent library
  * implementation of the same generator.  The FP8 NaN byte (R1) has no page
  * value behind it and is pinned to torch's float8 casts (both signs); the
- * 16-bit NaN pattern (R-NaN16) is a reading with no page or agreed library
- * value behind it: parity unpinned for that pattern beyond self-consistency.
+ * 16-bit NaN pattern (R-NaN16: every NaN becomes 0x7FFF, the image of the
+ * canonical binary32 NaN) is pinned to torch's CUDA FP16/BF16 casts of every
+ * binary32 NaN pattern and to the CPU libraries' image of 0x7FFFFFFF.
  */
 #ifndef MPNUM_ORACLE_H
 #define MPNUM_ORACLE_H

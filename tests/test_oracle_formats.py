@@ -71,8 +71,29 @@ def test_fp16_decode_matches_numpy_library():
     np.testing.assert_array_equal(ours[~nan].view(np.uint32), ref[~nan].view(np.uint32))
 
 
-def test_fp16_nan_is_canonical():
-    assert O.lib().orc_f32_to_f16(float("nan")) == 0x7FFF
+def all_f32_nans():
+    m = np.arange(1, 1 << 23, dtype=np.uint32)
+    return np.concatenate([0x7F800000 | m, 0xFF800000 | m]).view(np.float32)
+
+
+def test_16bit_nan_is_the_image_of_the_canonical_binary32_nan():
+    """Reading R-NaN16: every binary32 NaN, whatever its sign and payload, is
+    written as the 16-bit image of the canonical binary32 NaN 0x7FFFFFFF (the
+    NaN a GPU's arithmetic returns, so a NaN's bits never depend on which
+    operation made it).  That image is what numpy's and torch's CPU FP16
+    casts write for 0x7FFFFFFF, and in BF16, whose values are the upper
+    halves of binary32 values, the upper half 0x7FFF."""
+    canon = np.array([0x7FFFFFFF], np.uint32).view(np.float32)
+    f16_numpy = int(canon.astype(np.float16).view(np.uint16)[0])
+    f16_torch = int(torch.from_numpy(canon).to(torch.float16).view(torch.int16).numpy().view(np.uint16)[0])
+    bf16_upper_half = 0x7FFFFFFF >> 16
+    assert f16_numpy == f16_torch == 0x7FFF
+    nans = all_f32_nans()
+    assert (O.convert(nans, O.F32, O.F16) == f16_numpy).all()
+    assert (O.convert(nans, O.F32, O.BF16) == bf16_upper_half).all()
+    # and both decode to a NaN again
+    assert np.isnan(O.convert(np.array([f16_numpy], np.uint16), O.F16, O.F32)[0])
+    assert np.isnan(O.convert(np.array([bf16_upper_half], np.uint16), O.BF16, O.F32)[0])
 
 
 # ---- BF16 ---------------------------------------------------------------------
