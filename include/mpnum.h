@@ -329,14 +329,16 @@ MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, 
  * every device holds from library load to process exit; a call needs
  * nvfp4_workspace_size() bytes of it and returns MP_EWORKSPACE if that is
  * more than the array holds.  The call allocates and frees nothing.
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current: make that first call
- * before any stream capture.  Each call first clears the words that must
- * start at zero (a stream-ordered memset of the library's own scratch; this
- * happens before the argument checks, which otherwise behave as in
- * nvfp4_quantize).  Every call on a device shares the one array: calls that
- * overlap on the GPU (different streams, no ordering between them) race on it
- * and their results are undefined. */
+ * Arguments are checked first, exactly as in nvfp4_quantize, and an argument
+ * error returns before anything is enqueued.  The first call in each CUDA
+ * context (each device's primary context, and again after cudaDeviceReset
+ * makes a new one) looks up the array's device address (cudaGetSymbolAddress)
+ * with that context current: make that first call before any stream capture.
+ * Each call then clears the words that must start at zero (a stream-ordered
+ * memset of the library's own scratch) and enqueues the two kernels.  Every
+ * call on a device shares the one array: calls that overlap on the GPU
+ * (different streams, no ordering between them) race on it and their results
+ * are undefined. */
 MP_API size_t nvfp4_noalloc_scratch_bytes(void);
 MP_API mp_status nvfp4_quantize_noalloc(const void* x_bf16, int64_t rows, int64_t cols,
                                         int32_t block_2d, int32_t stochastic, uint64_t seed,

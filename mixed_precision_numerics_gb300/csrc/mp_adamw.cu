@@ -567,10 +567,6 @@ bool finite_f(float x) { return x == x && x - x == 0.0f; }
 }  // namespace
 }  // namespace mp
 
-extern "C" {
-
-}  // extern "C"
-
 namespace mp {
 namespace {
 

@@ -537,9 +537,35 @@ void dispatch_deq(bool deq, bool block_2d, const uint16_t* x, int64_t rows, int6
 }  // namespace
 }  // namespace mp
 
+namespace mp {
+namespace {
+
+constexpr size_t kNvfp4WorkspaceBytes = 256;
+
+// The argument checks of both quantiser entry points, run before a call
+// enqueues anything.  need_ws: the caller passes a workspace to be checked
+// (nvfp4_quantize); the no-alloc entry point has its own scratch.
+mp_status nvfp4_check_args(const void* x_bf16, int64_t rows, int64_t cols, int32_t block_2d, const uint8_t* codes,
+                           const uint8_t* block_scales, const float* d_tensor_scale, const int32_t* d_nonfinite,
+                           const void* dequant_bf16, bool need_ws, const void* d_workspace, size_t workspace_bytes) {
+  if (rows < 0 || cols < 0 || !d_tensor_scale || !d_nonfinite) return MP_EINVAL;
+  const int64_t n = rows * cols;
+  if (n > 0 && (!x_bf16 || !codes || !block_scales)) return MP_EINVAL;
+  if (cols % 16 != 0 || (block_2d && rows % 16 != 0)) return MP_ESHAPE;
+  if (need_ws && (!d_workspace || workspace_bytes < kNvfp4WorkspaceBytes)) return MP_EWORKSPACE;
+  if ((n > 0 && (!aligned16(x_bf16) || !aligned16(codes))) || (dequant_bf16 && !aligned16(dequant_bf16)) ||
+      (reinterpret_cast<uintptr_t>(d_tensor_scale) & 3u) || (reinterpret_cast<uintptr_t>(d_nonfinite) & 3u) ||
+      (need_ws && (reinterpret_cast<uintptr_t>(d_workspace) & 7u)))
+    return MP_EALIGN;
+  return MP_OK;
+}
+
+}  // namespace
+}  // namespace mp
+
 extern "C" {
 
-MP_API size_t nvfp4_workspace_size(void) { return 256; }
+MP_API size_t nvfp4_workspace_size(void) { return mp::kNvfp4WorkspaceBytes; }
 
 MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, int32_t block_2d,
                                 int32_t stochastic, uint64_t seed, int32_t apply_rht, uint16_t rht_sign_mask,
@@ -547,15 +573,10 @@ MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, 
                                 int32_t* d_nonfinite, void* dequant_bf16, void* d_workspace,
                                 size_t workspace_bytes, void* stream) {
   using namespace mp;
-  if (rows < 0 || cols < 0 || !d_tensor_scale || !d_nonfinite) return MP_EINVAL;
+  const mp_status bad = nvfp4_check_args(x_bf16, rows, cols, block_2d, codes, block_scales, d_tensor_scale,
+                                         d_nonfinite, dequant_bf16, true, d_workspace, workspace_bytes);
+  if (bad != MP_OK) return bad;
   const int64_t n = rows * cols;
-  if (n > 0 && (!x_bf16 || !codes || !block_scales)) return MP_EINVAL;
-  if (cols % 16 != 0 || (block_2d && rows % 16 != 0)) return MP_ESHAPE;
-  if (!d_workspace || workspace_bytes < nvfp4_workspace_size()) return MP_EWORKSPACE;
-  if ((n > 0 && (!aligned16(x_bf16) || !aligned16(codes))) || (dequant_bf16 && !aligned16(dequant_bf16)) ||
-      (reinterpret_cast<uintptr_t>(d_tensor_scale) & 3u) || (reinterpret_cast<uintptr_t>(d_nonfinite) & 3u) ||
-      (reinterpret_cast<uintptr_t>(d_workspace) & 7u))
-    return MP_EALIGN;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   Ws* ws = static_cast<Ws*>(d_workspace);
@@ -609,8 +630,10 @@ MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t 
 // library a workspace.  Its scratch is this file-scope device array, created
 // when the library is loaded on each device and kept until the process exits.
 // Host code may not take the array's address directly (the name is a host-side
-// stand-in); the device address is looked up once per device with
-// cudaGetSymbolAddress, with that device current.
+// stand-in); the device address is looked up with cudaGetSymbolAddress the
+// first time each CUDA context calls, with that context current, and kept by
+// the context's id, so a device reset (a new context, where the module and
+// its array may sit elsewhere) looks it up again.
 // ---------------------------------------------------------------------------
 namespace mp {
 namespace {
@@ -618,21 +641,65 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = 256;
 __device__ __align__(256) unsigned char g_nvfp4_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+static_assert(kNvfp4WorkspaceBytes <= kNoAllocScratchBytes, "the scratch array holds one call's workspace");
 
-mp_status noalloc_scratch_for_current_device(void** out) {
+// The driver's id of the current context, reached through the runtime (no
+// link against the driver library).  Ids are unique for the life of the
+// process, so a context destroyed and created again (cudaDeviceReset) gets a
+// new one even where its handle is reused.
+bool current_context_id(unsigned long long* id) {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static std::atomic<void*> get_current{nullptr}, get_id{nullptr};
+  void* gc = get_current.load(std::memory_order_acquire);
+  void* gi = get_id.load(std::memory_order_acquire);
+  if (!gc || !gi) {
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &gc, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !gc)
+      return false;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &gi, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !gi)
+      return false;
+    get_current.store(gc, std::memory_order_release);
+    get_id.store(gi, std::memory_order_release);
+  }
+  CUcontext ctx = nullptr;
+  if (reinterpret_cast<GetCurrent>(gc)(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return reinterpret_cast<GetId>(gi)(ctx, id) == CUDA_SUCCESS;
+}
+
+// The array's device address in the current context, looked up with
+// cudaGetSymbolAddress the first time a context calls and kept per context id.
+constexpr int kMaxContexts = 64;
+std::mutex g_scratch_mu;
+struct ScratchEntry {
+  unsigned long long ctx_id;
+  void* addr;
+};
+ScratchEntry g_scratch[kMaxContexts] = {};
+int g_scratch_used = 0;
+
+mp_status noalloc_scratch_for_current_context(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return MP_ECUDA;
-  if (dev < 0 || dev >= kMaxDevices) return MP_EINVAL;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_nvfp4_noalloc_scratch) != cudaSuccess || !p) return MP_ECUDA;
-    g_scratch_addr[dev] = p;
+  unsigned long long id = 0;
+  if (!current_context_id(&id)) {
+    // No context is current on this thread yet: the runtime would use the
+    // device's primary context, which cudaSetDevice makes current.
+    if (cudaSetDevice(dev) != cudaSuccess || !current_context_id(&id)) return MP_ECUDA;
   }
-  *out = g_scratch_addr[dev];
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  for (int i = 0; i < g_scratch_used; ++i)
+    if (g_scratch[i].ctx_id == id) {
+      *out = g_scratch[i].addr;
+      return MP_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_nvfp4_noalloc_scratch) != cudaSuccess || !p) return MP_ECUDA;
+  const int slot = g_scratch_used < kMaxContexts ? g_scratch_used++ : (int)(id % kMaxContexts);
+  g_scratch[slot] = ScratchEntry{id, p};
+  *out = p;
   return MP_OK;
 }
 
@@ -647,11 +714,15 @@ extern "C" MP_API mp_status nvfp4_quantize_noalloc(const void* x_bf16, int64_t r
                                                    uint8_t* block_scales, float* d_tensor_scale,
                                                    int32_t* d_nonfinite, void* dequant_bf16, void* stream) {
   using namespace mp;
+  // Every argument is checked before anything is enqueued or looked up.
+  const mp_status bad = nvfp4_check_args(x_bf16, rows, cols, block_2d, codes, block_scales, d_tensor_scale,
+                                         d_nonfinite, dequant_bf16, false, nullptr, 0);
+  if (bad != MP_OK) return bad;
   // A call needs nvfp4_workspace_size() bytes of scratch; the fixed array
   // must hold that much.
   if (nvfp4_workspace_size() > kNoAllocScratchBytes) return MP_EWORKSPACE;
   void* scratch = nullptr;
-  const mp_status rc = noalloc_scratch_for_current_device(&scratch);
+  const mp_status rc = noalloc_scratch_for_current_context(&scratch);
   if (rc != MP_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The accumulator and ticket must start at zero; clear them in stream order.

@@ -97,6 +97,15 @@ def test_argument_validation_without_gpu(M):
     assert q(16, 8, 32, 1, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
     assert q(16, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 4, None) == M.MP_EWORKSPACE
     assert q(8, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_EALIGN
+    # the no-alloc quantiser checks its arguments before it touches CUDA at
+    # all: here, with no GPU, every argument error is reported as such
+    qa = L.nvfp4_quantize_noalloc
+    assert qa(16, 2, 24, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, None) == M.MP_ESHAPE
+    assert qa(16, 8, 32, 1, 0, 0, 0, 0, 16, 16, 16, 16, None, None) == M.MP_ESHAPE
+    assert qa(None, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, None) == M.MP_EINVAL
+    assert qa(16, -1, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, None) == M.MP_EINVAL
+    assert qa(8, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, None) == M.MP_EALIGN
+    assert qa(16, 2, 32, 0, 0, 0, 0, 0, 16, 16, 16, 16, 24, None) == M.MP_EALIGN
     assert L.rht16(16, 2, 40, 0, 16, M.MP_F32, None) == M.MP_ESHAPE
     assert L.rht16(16, 2, 32, 0, 16, M.MP_E4M3, None) == M.MP_EINVAL
     mx = L.mx_quantize
