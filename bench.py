@@ -25,7 +25,6 @@ import ctypes
 import hashlib
 import json
 import os
-import re
 import statistics
 import subprocess
 import sys
@@ -201,19 +200,27 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic_per_param():
-    """DRAM bytes per parameter of the update kernel from the committed ncu
-    summary, or None when that summary was taken on different kernel source."""
-    path = os.path.join(ROOT, "profiles", "adamw_update_llama3_8b.md")
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "adamw_update_traffic.json")
+
+
+def profiled_traffic(params: int):
+    """DRAM bytes of one update launch over `params` parameters, from the
+    committed ncu record of a smaller capture of the same kernel, or None when
+    that record was taken on different kernel source.  Reads scale with the
+    parameters (the capture read exactly 14 B/param); writes are 14 B/param
+    less the bytes the capture left dirty in L2 at kernel end (a constant of
+    the cache, not of the parameter count).  Returns (read, write, residue)."""
     try:
-        text = open(path).read()
-    except OSError:
+        with open(TRAFFIC_RECORD) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
         return None
-    m = re.search(r"dram_bytes_per_param:\s*([0-9.]+)", text)
-    s = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    if not m or not s or s.group(1) != kernel_source_hash():
+    if rec.get("kernel_source_sha") != kernel_source_hash():
         return None
-    return float(m.group(1))
+    n = rec["capture_params"]
+    read = rec["dram_bytes_read"] / n * params
+    residue = B_APPLY / 2 * n - rec["dram_bytes_write"]
+    return read, B_APPLY / 2 * params - residue, residue
 
 
 # ---------------------------------------------------------------------------------------
@@ -765,9 +772,14 @@ def run_reference(args):
     value = OracleSample.combined(samples).projected(full)
     sample = (f"{n} threads, each: " + samples[0].describe().replace("oracle, 1 thread: ", "") +
               f"; {args.steps} timed sample steps in {elapsed:.1f} s")
+    # ms_per_step is the wall time of one timed sample step (every thread's
+    # bounded sample); the full step's time at the measured rates is reported
+    # under its own key.
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(sum(full.values()) / (value * 1e9) * 1e3, 3),
+            "ms_per_step": round(elapsed / max(args.steps, 1) * 1e3, 3),
+            "sample_bytes_per_step": int(sum(s.sample_bytes() for s in samples) / max(args.steps, 1)),
+            "projected_ms_per_full_step": round(sum(full.values()) / (value * 1e9) * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAME, "arm": f"CPU oracle (scalar C, -O2) on {n} host threads"},
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": n, "kind": "oracle", "sample": sample},
@@ -850,11 +862,17 @@ def main():
 
     apply_ms = per_call_ms["adamw_apply"]
     achieved = wl.bytes["adamw_apply"] / (apply_ms * 1e-3) / 1e9
-    tpp = profiled_traffic_per_param()
+    tr = profiled_traffic(wl.P)
     roofline = {"bound": "hbm", "kernel": "k_adamw_update (mp_adamw_apply, 28 B/param)",
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
-                "traffic": round(tpp * wl.P) if tpp else None}
+                "traffic": round(tr[0] + tr[1]) if tr else None}
+    if tr:
+        roofline["traffic_read"] = round(tr[0])
+        roofline["traffic_write"] = round(tr[1])
+        roofline["traffic_note"] = (f"from {os.path.relpath(TRAFFIC_RECORD, ROOT)}: reads scaled by params "
+                                    f"(the capture read {B_APPLY / 2:.0f} B/param); writes {B_APPLY / 2:.0f} B/param "
+                                    f"less {tr[2] / 1e6:.1f} MB left dirty in L2 at kernel end (not scaled)")
 
     # Each quantiser call alone: 16 back-to-back calls captured in a CUDA
     # graph and replayed after an L2-clean point, so neither launch gaps nor
