@@ -3,8 +3,8 @@
 Covers every BF16 bit pattern at several scales, F16 and F32 inputs with
 specials, ragged lengths, the tiny delayed-scaling workload (1024x1024 BF16,
 history 16, 20 iterations) element by element, the FP8 workload at reduced
-row count element by element, and the full [8192 x 4096] workload with
-sampled elements plus the exact amax/scale recurrence.
+row count element by element, and the full [8192 x 4096] workload byte for
+byte in every one of its 64 iterations, with the exact amax/scale recurrence.
 """
 import ctypes
 
@@ -149,12 +149,25 @@ def test_fp8_workload_reduced_rows(which):
     run_sequence(recipes, rows, c.cols, fmt, c.hist_len, c.margin)
 
 
+def oracle_cast_parallel(x_host, x_fmt, fmt, scale):
+    """The oracle's cast over row chunks on the host threads (its C calls
+    release the GIL); the cast is element-wise, so chunking changes nothing."""
+    import concurrent.futures as cf
+
+    from tests.gpu_util import threads
+
+    parts = np.array_split(x_host, threads() * 2)
+    with cf.ThreadPoolExecutor(threads()) as ex:
+        return np.concatenate(list(ex.map(lambda p: O.fp8_cast_array(p, x_fmt, fmt, scale), parts)))
+
+
 @pytest.mark.parametrize("which", ["act", "grad"])
-def test_fp8_workload_full_size_sampled(which):
-    """[8192 x 4096] x 64 iterations: the amax of each iteration is checked
-    against torch's max |x| (exact), the scale recurrence against the oracle
-    fed those amaxes, and 65536 sampled bytes per iteration against the
-    oracle's cast of the host-regenerated inputs."""
+def test_fp8_workload_full_size(which):
+    """[8192 x 4096] x 64 iterations: every output byte of every iteration
+    against the oracle's cast of the same input under the scale in force, the
+    amax of each iteration against torch's max |x| (exact), the scale
+    recurrence against the oracle fed those amaxes, and the first 65536
+    inputs of each iteration against the host generator."""
     c = W.FP8
     n = c.rows * c.cols
     fmt = M.MP_E4M3 if which == "act" else M.MP_E5M2
@@ -163,31 +176,24 @@ def test_fp8_workload_full_size_sampled(which):
     x = torch.empty(n, dtype=torch.bfloat16, device="cuda")
     y = torch.empty(n, dtype=torch.uint8, device="cuda")
     om, oh = O.new_fp8_meta(), np.zeros(c.hist_len, np.float32)
-    rng = np.random.default_rng(0)
-    sat = 0
+    sat, scale_changes = 0, 0
     for k in range(c.iters):
         r = c.act_recipe(k) if which == "act" else c.grad_recipe(k)
         synth.fill_device(r, synth.BF16, x)
         scale_in_force = om.scale
         M.fp8_cast_delayed(x, y, fmt, meta, hist, c.margin)
+        x_host = to_host(x, np.uint16)
+        np.testing.assert_array_equal(x_host[:65536], synth.fill(r, synth.BF16, 65536))
+        ref = oracle_cast_parallel(x_host, O.BF16, FMT[fmt], scale_in_force)
+        got = y.cpu().numpy()
+        bad = np.flatnonzero(got != ref)
+        assert bad.size == 0, f"iteration {k}: {bad.size} bytes differ, first at {bad[:5]}"
         amax = float(x.float().abs().max().item())
-        idx = np.sort(rng.choice(n, 65536, replace=False))
-        idx_t = torch.from_numpy(idx).cuda()
-        y_s = y[idx_t].cpu().numpy()
-        x_s = synth.fill_at(r, synth.BF16, idx)
-        np.testing.assert_array_equal(x_s, to_host(x[idx_t], np.uint16))
-        ref = O.fp8_cast_array(x_s, O.BF16, FMT[fmt], scale_in_force)
-        assert np.array_equal(y_s, ref), f"iteration {k}"
         O.fp8_history_update(om, oh, c.margin, amax, FMT[fmt])
         assert_meta_equal(M.read_fp8_meta(meta), om)
-        # Whole-tensor property: a byte is the largest code exactly when
-        # |x * scale| rounds to it or beyond (the tie at the midpoint below the
-        # top goes to the even code: up for E4M3, down for E5M2).
-        p = (x.float() * scale_in_force).abs()
-        top = (y & 0x7F) == (0x7E if fmt == M.MP_E4M3 else 0x7B)
-        expect = (p >= 432.0) if fmt == M.MP_E4M3 else (p > 53248.0)
-        assert torch.equal(top, expect), f"iteration {k}: saturation pattern"
-        sat += int(top.sum().item())
+        scale_changes += int(om.scale != scale_in_force)
+        sat += int(((ref & 0x7F) == (0x7E if fmt == M.MP_E4M3 else 0x7B)).sum())
+    assert scale_changes > 0
     if which == "act":
         assert sat > 0  # the drifting std makes the delayed scale lag: saturation happens
 
