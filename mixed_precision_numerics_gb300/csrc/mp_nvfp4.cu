@@ -49,7 +49,7 @@ struct Ws {
 // gives both sums and one packed fma(b, -1, a) both differences (the product
 // by -1 is exact, so the fma rounds a - b once, as the subtraction does); the
 // stage of distance 8 works inside each pair.
-__device__ __forceinline__ void fwht16_packed(float2 (&p)[8]) {
+__device__ __forceinline__ void fwht16_first3(float2 (&p)[8]) {
   const float2 m1 = make_float2(-1.0f, -1.0f);
 #pragma unroll
   for (int h = 1; h < 8; h <<= 1) {
@@ -61,11 +61,17 @@ __device__ __forceinline__ void fwht16_packed(float2 (&p)[8]) {
       p[i + h] = __ffma2_rn(b, m1, a);
     }
   }
+}
+__device__ __forceinline__ void fwht16_last(float2 (&p)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const float a = p[i].x, b = p[i].y;
     p[i] = make_float2(__fadd_rn(a, b), __fsub_rn(a, b));
   }
+}
+__device__ __forceinline__ void fwht16_packed(float2 (&p)[8]) {
+  fwht16_first3(p);
+  fwht16_last(p);
 }
 
 // x' of one 16-element BF16 tile (two 16-byte words) as the pairs
@@ -100,7 +106,8 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restr
   __shared__ int is_last;
   const SignWords sw = sign_words(mask);
   float acc = 0.0f;
-  constexpr int U = 2;
+  uint32_t pm = 0u;            // without the transform: max |x| of BF16 pairs, packed
+  constexpr int U = RHT ? 2 : 4;  // 32-byte tiles in flight per thread
   const uint64_t keep = policy_evict_last();
   const int64_t step = (int64_t)gridDim.x * kThreads * U;
   for (int64_t t0 = (int64_t)blockIdx.x * kThreads * U + threadIdx.x; t0 < ntiles; t0 += step) {
@@ -122,15 +129,40 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_amax(const uint16_t* __restr
     for (int u = 0; u < U; ++u) {
       const int64_t t = t0 + (int64_t)u * kThreads;
       if (t >= ntiles) continue;
-      float2 p[8];
-      tile_pairs<RHT, false>(a[u], b[u], sw, p);  // the 1/4 is applied once to the maximum below
+      if (RHT) {
+        // The last butterfly stage maps each pair (a, b) to a + b and a - b,
+        // the larger magnitude being RN(|a| + |b|); so the first three stages
+        // and one add per pair give the tile's max |v| (the 1/4 is applied
+        // once to the maximum below).  Only infinite a and b together make a
+        // NaN output where that sum is infinite: such a tile takes the last
+        // stage in full.
+        float2 p[8];
+        apply_signs(a[u], b[u], sw);
+        const uint32_t w[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        acc = max_abs_nan(acc, p[j].x);
-        acc = max_abs_nan(acc, p[j].y);
+        for (int i = 0; i < 8; ++i) {
+          const float lo = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+          const float hi = (i & 1) ? bf16hi(w[4 + (i >> 1)]) : bf16lo(w[4 + (i >> 1)]);
+          p[i] = make_float2(lo, hi);
+        }
+        fwht16_first3(p);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = max_abs_nan(m, __fadd_rn(fabsf(p[j].x), fabsf(p[j].y)));
+        if (__builtin_expect(isinf(m), 0)) {
+          fwht16_last(p);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) m = max_abs_nan(max_abs_nan(m, p[j].x), p[j].y);
+        }
+        acc = max_abs_nan(acc, m);
+      } else {
+        const uint32_t w[8] = {a[u].x, a[u].y, a[u].z, a[u].w, b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) pm = max_abs_nan_x2<true>(pm, w[k]);
       }
     }
   }
+  if (!RHT) acc = max_abs_nan(max_abs_nan(acc, bf16lo(pm)), bf16hi(pm));
   const uint32_t cta = block_max_u32(amax_bits(acc), red);
   if (threadIdx.x == 0) {
     atomicMax(&ws->amax_bits, cta);
@@ -193,43 +225,57 @@ __device__ __forceinline__ uint32_t sr_e2m1(float y, uint32_t r16) {
   return (((__float_as_uint(b) + r16 * 64u) >> 22) - 252u) + sign;  // magnitude <= 7: + is |
 }
 
-// Encode a 16-element tile of x', held as pairs (x'[i], x'[i + 8]), with block
-// reciprocal r; returns 8 packed bytes.  The products x' * r are formed two at
-// a time (packed binary32 multiply, each rounded as __fmul_rn).  `flat` is the
-// flat index of the first element (a multiple of 16).
-template <bool SR>
-__device__ __forceinline__ uint2 encode16p(const float2 (&p)[8], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
-  float y[16];
+// prmt.b32: result byte i is byte (sel nibble i & 7) of {b, a}; a nibble with
+// bit 3 set gives that byte's top bit copied into all eight bits.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// The sign bits of 8 floats g[j], at bit 4j + 3 (the sign bit of nibble j),
+// in a word whose other bits are junk (the caller masks with 0x88888888):
+// bit 7 of byte k is the top bit of g[2k + 1]; bits 0-6 copy the sign of g[2k].
+__device__ __forceinline__ uint32_t nibble_signs(const float (&g)[8]) {
+  const uint32_t o = prmt(prmt(__float_as_uint(g[1]), __float_as_uint(g[3]), 0x0073u),
+                          prmt(__float_as_uint(g[5]), __float_as_uint(g[7]), 0x7300u), 0x7610u);
+  const uint32_t e = prmt(prmt(__float_as_uint(g[0]), __float_as_uint(g[2]), 0x00FBu),
+                          prmt(__float_as_uint(g[4]), __float_as_uint(g[6]), 0xFB00u), 0x7610u);
+  return (o & 0x80808080u) | (e & 0x7F7F7F7Fu);
+}
+
+// Stochastic E2M1 codes of 8 values y[j] and the four 32-bit words of one
+// Philox call (element j takes 16-bit half j mod 2 of word j / 2); element j
+// goes to nibble j.  The rule, round away from zero iff floor(frac * 2^16) +
+// r16 >= 2^16, on binary32 bits: z = RZ(min(|y|, 6) * 2^-126) places the E2M1
+// grid on binary32's own: |y| < 1 becomes a subnormal with |y| * 2^23 in its
+// bits (spacing 0.5 at bit 22, like E2M1's subnormals), and |y| in [1, 2),
+// [2, 4), [4, 6] the binades of exponent field 1, 2, 3 with the kept mantissa
+// bit at 22.  So bits 22-24 of z are the code rounded toward zero and bits
+// 6-21 are floor(frac * 2^16); (bits(z) + r16 * 2^6) >> 22 is the code after
+// the rule's carry.  The truncating multiply keeps every bit the rule reads
+// (|y| down to 2^-23).  Signs come from y's sign bits.  The adds and shifts
+// here run on the integer pipes, leaving the multiply pipe to Philox.
+__device__ __forceinline__ uint32_t sr_group(const float (&y)[8], u32x4 R) {
+  const uint32_t w[4] = {R.x, R.y, R.z, R.w};
+  float a[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float2 q = __fmul2_rn(p[i], make_float2(r, r));
-    y[i] = q.x;
-    y[i + 8] = q.y;
+  for (int j = 0; j < 8; ++j) a[j] = fminf(fabsf(y[j]), 6.0f);
+  uint32_t zb[8];
+#pragma unroll
+  for (int j = 0; j < 8; j += 2) {
+    const float2 z = __fmul2_rz(make_float2(a[j], a[j + 1]), make_float2(0x1p-126f, 0x1p-126f));
+    zb[j] = __float_as_uint(z.x);
+    zb[j + 1] = __float_as_uint(z.y);
   }
-  uint32_t lo = 0, hi = 0;
-  if (SR) {
-    const uint64_t g = flat >> 3;
-    const u32x4 R0 = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
-    const uint64_t g1 = g + 1;
-    const u32x4 R1 = philox4x32_10((uint32_t)g1, (uint32_t)(g1 >> 32), 0u, 0u, k0, k1);
-    const uint32_t words[8] = {R0.x, R0.y, R0.z, R0.w, R1.x, R1.y, R1.z, R1.w};
+  uint32_t acc = 0;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const uint32_t w = words[j >> 1];
-      const uint32_t r16 = (j & 1) ? (w >> 16) : (w & 0xFFFFu);
-      const uint32_t c = sr_e2m1(y[j], r16);
-      if (j < 8) lo += c << (4 * j);  // disjoint nibbles: + is |
-      else hi += c << (4 * (j - 8));
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const uint32_t c = cvt_e2m1x2(y[2 * k], y[2 * k + 1]);
-      if (k < 4) lo |= c << (8 * k);
-      else hi |= c << (8 * (k - 4));
-    }
+  for (int j = 7; j >= 0; --j) {
+    const uint32_t word = w[j >> 1];
+    const uint32_t r6 = (j & 1) ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u);  // r16 * 2^6
+    acc = acc * 16u + ((zb[j] + r6) >> 22);
   }
-  return make_uint2(lo, hi);
+  return acc | (nibble_signs(y) & 0x88888888u);
 }
 
 // BF16 RNE of value(code) * d for the 16 codes in (lo, hi).
@@ -244,6 +290,52 @@ __device__ __forceinline__ void dequant16(uint2 q, float d, uint16_t* out) {
   st_cs(out + 8, make_uint4(w[4], w[5], w[6], w[7]));
 }
 
+// Per-CTA table, one entry per E4M3 block-scale code c: d = value(c) * s_t and
+// the multiplier that turns the tile's values into y = x' * r, r = 1/d (0 when
+// d is 0 or 1/d is not finite).  With the transform the multiplier applies to
+// the butterfly's output before its 1/4, so it is r/4: an exact scaling while
+// 2^-90 <= s_t <= 2^110 (r between 2^-119 and 2^99), and the product equals
+// the oracle's two-step one except for elements below 2^-124, whose codes are
+// zero either way (|y| < 2^-27, below any rounding step or random carry).
+template <bool RHT>
+__device__ __forceinline__ void fill_scale_table(float2* tab, float s_t) {
+  for (int c = threadIdx.x; c < 128; c += kThreads) {
+    const float d = __fmul_rn(e4m3_pos_to_f32((uint32_t)c), s_t);
+    float r = 0.0f;
+    if (d != 0.0f) {
+      const float inv = __fdiv_rn(1.0f, d);
+      if (isfinite(inv)) r = inv;
+    }
+    if (RHT) r = __fmul_rn(r, 0.25f);
+    tab[c] = make_float2(d, r);
+  }
+}
+
+// Tile of 16 BF16 values (two 16-byte words) as the pairs (x[i], x[i + 8]),
+// with the random signs of the transform applied: the low half of a word
+// becomes w * 2^16 plus the sign (adding 2^31 flips the top bit), the high
+// half (w ^ sign word) with the low half cleared.
+template <bool RHT>
+__device__ __forceinline__ void unpack_tile(uint4 a, uint4 b, const SignWords& sw, const uint32_t (&slo)[8],
+                                            float2 (&p)[8]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  float v[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    v[2 * k] = __uint_as_float(RHT ? w[k] * 65536u + slo[k] : w[k] << 16);
+    v[2 * k + 1] = __uint_as_float((RHT ? (w[k] ^ sw.w[k]) : w[k]) & 0xFFFF0000u);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) p[i] = make_float2(v[i], v[i + 8]);
+}
+
+// One 16-element block per thread per step.  Block scale: q~ = bamax * K with
+// K = RN(RN(1/6) * RN(1/s_t)) lies within 6.01 units of 2^-24 (relative) of
+// q = RN(RN(bamax / 6) / s_t) when everything is normal, so if the E4M3
+// conversions of q~ * (1 - 2^-21) and q~ * (1 + 2^-21) agree, that code is
+// the code of q (conversion is monotonic); tiny or non-normal cases, and the
+// rare disagreement, take the exact divisions.  The code then indexes the
+// per-CTA table for d and the multiplier.
 template <bool RHT, bool SR, bool DEQ>
 __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restrict__ x, int64_t nblocks,
                                                          uint32_t mask, uint64_t seed,
@@ -251,11 +343,19 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
                                                          const int32_t* __restrict__ nonfinite,
                                                          uint8_t* __restrict__ codes, uint8_t* __restrict__ scales,
                                                          uint16_t* __restrict__ deq) {
+  __shared__ float2 tab[128];
   chain_wait();  // the previous kernel in the stream has finished and its writes are visible
   chain_release();
   const float s_t = *tensor_scale;
   const bool zero = (*nonfinite != 0) || s_t == 0.0f;
+  fill_scale_table<RHT>(tab, s_t);
+  __syncthreads();
+  const bool fast = s_t >= 0x1p-90f && s_t <= 0x1p110f;
+  const float K = __fmul_rn(__fdiv_rn(1.0f, 6.0f), __fdiv_rn(1.0f, s_t));
   const SignWords sw = sign_words(mask);
+  uint32_t slo[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) slo[k] = sw.w[k] << 16;
   const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
   const int64_t stride = (int64_t)gridDim.x * kThreads;
   const uint64_t last_use = policy_evict_first();  // this pass is the last reader of x
@@ -271,16 +371,79 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
       }
       continue;
     }
+    const uint4 ca = ld_hint(x + blk * 16, last_use), cb = ld_hint(x + blk * 16 + 8, last_use);
     float2 p[8];
-    tile_pairs<RHT>(ld_hint(x + blk * 16, last_use), ld_hint(x + blk * 16 + 8, last_use), sw, p);
-    float bamax = 0.0f;
+    unpack_tile<RHT>(ca, cb, sw, slo, p);
+    float bamax;
+    if (RHT) {
+      // The last butterfly stage turns each pair (a, b) into a + b and a - b,
+      // the larger in magnitude being RN(|a| + |b|) (rounding is monotonic and
+      // symmetric), so the block's max |v| is the max of those eight sums; and
+      // max |x'| = RN(max |v| / 4).
+      fwht16_first3(p);
+      float m[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) bamax = fmaxf(bamax, fmaxf(fabsf(p[j].x), fabsf(p[j].y)));
-    const BlockScale bs = block_scale(bamax, s_t);
-    const uint2 q = encode16p<SR>(p, bs.r, (uint64_t)blk * 16, k0, k1);
+      for (int j = 0; j < 8; ++j) m[j] = __fadd_rn(fabsf(p[j].x), fabsf(p[j].y));
+      fwht16_last(p);
+      bamax = __fmul_rn(fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7]))),
+                        0.25f);
+    } else {
+      // max |x| on the packed BF16 words (exact)
+      const uint32_t w[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+      uint32_t m = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m = max_abs_nan_x2<true>(m, w[k]);
+      bamax = fmaxf(bf16lo(m), bf16hi(m));
+    }
+    uint32_t code = 0;
+    bool ok = fast && (bamax >= 0x1p-120f || bamax == 0.0f);
+    if (ok) {
+      const float qt = __fmul_rn(bamax, K);
+      const uint32_t c2 = cvt_e4m3x2(__fmul_rn(qt, 1.0f - 0x1p-21f), __fmul_rn(qt, 1.0f + 0x1p-21f));
+      code = c2 & 0xFFu;
+      ok = code == (c2 >> 8);
+    }
+    float d;
+    float2 y[8];
+    if (ok) {
+      const float2 e = tab[code];
+      d = e.x;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) y[j] = __fmul2_rn(p[j], make_float2(e.y, e.y));
+    } else {
+      const BlockScale bs = block_scale(bamax, s_t);
+      code = bs.code;
+      d = bs.d;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 xq = RHT ? __fmul2_rn(p[j], make_float2(0.25f, 0.25f)) : p[j];
+        y[j] = __fmul2_rn(xq, make_float2(bs.r, bs.r));
+      }
+    }
+    uint2 q;
+    if (SR) {
+      const uint64_t g = (uint64_t)blk * 2;  // counter of elements 16 blk .. 16 blk + 7
+      const u32x4 R0 = philox4x32_10((uint32_t)g, (uint32_t)(g >> 32), 0u, 0u, k0, k1);
+      const u32x4 R1 = philox4x32_10((uint32_t)(g + 1), (uint32_t)((g + 1) >> 32), 0u, 0u, k0, k1);
+      float g0[8], g1[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        g0[j] = y[j].x;
+        g1[j] = y[j].y;
+      }
+      q = make_uint2(sr_group(g0, R0), sr_group(g1, R1));
+    } else {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lo |= cvt_e2m1x2(y[2 * k].x, y[2 * k + 1].x) << (8 * k);
+        hi |= cvt_e2m1x2(y[2 * k].y, y[2 * k + 1].y) << (8 * k);
+      }
+      q = make_uint2(lo, hi);
+    }
     __stcs(reinterpret_cast<uint2*>(codes + blk * 8), q);
-    scales[blk] = (uint8_t)bs.code;
-    if (DEQ) dequant16(q, bs.d, deq + blk * 16);
+    scales[blk] = (uint8_t)code;
+    if (DEQ) dequant16(q, d, deq + blk * 16);
   }
 }
 
