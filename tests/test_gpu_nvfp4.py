@@ -222,3 +222,73 @@ def test_random_shape_sweep_2d_against_the_oracle():
         got = gpu_quant(x, True, sr, 77 + i, rht, 0x5A3C)
         ref = O.nvfp4_quantize(x, True, sr, 77 + i, rht, 0x5A3C)
         assert_same(got, ref, f"{rows}x{cols} sr={sr} rht={rht}")
+
+
+# ---- the 1x16 encode's division-free block scale and its exact fallback -----------
+
+
+def _bf16(v):
+    return O.convert(np.asarray(v, np.float32), O.F32, O.BF16)
+
+
+def midpoint_blocks(amax_bf16: int, count: int):
+    """BF16 block maxima b whose block-scale quotient q = RN(RN(b / 6) / s_t)
+    lies within a few units of an E4M3 rounding midpoint under the tensor
+    scale s_t of a tensor with max |x| = amax: the blocks for which the
+    encode's division-free estimate of the scale code cannot decide and the
+    exact divisions run.  Found by the oracle's arithmetic in numpy."""
+    f = np.float32
+    a = O.convert(np.array([amax_bf16], np.uint16), O.BF16, O.F32)[0]
+    s_t = f(a) / f(2688.0)
+    b = O.convert(np.arange(1, amax_bf16 + 1, dtype=np.uint16), O.BF16, O.F32)
+    qt = b * ((f(1) / f(6)) * (f(1) / s_t))
+    lo, hi = qt * f(1 - 2.0 ** -21), qt * f(1 + 2.0 ** -21)
+    undecided = O.convert(lo, O.F32, O.E4M3) != O.convert(hi, O.F32, O.E4M3)
+    return np.arange(1, amax_bf16 + 1, dtype=np.uint16)[undecided][:count]
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_1x16_blocks_whose_scale_code_needs_the_exact_divisions(sr):
+    amax = int(_bf16([3.5])[0])  # a tensor max with many undecided block maxima (126)
+    mids = midpoint_blocks(amax, 512)
+    assert mids.size >= 100, "too few undecided block maxima for this tensor max"
+    rng = np.random.default_rng(17)
+    rows = mids.size + 1
+    x = synth.fill(synth.recipe(80, 0, 0.05), synth.BF16, rows * 16, shape=(rows, 16))
+    x[0, 5] = amax  # the tensor max
+    for r, m in enumerate(mids, start=1):
+        x[r, rng.integers(0, 16)] = m | (0x8000 if r % 3 == 0 else 0)  # the block max, some negative
+        over = np.abs(O.convert(x[r], O.BF16, O.F32)) > O.convert(np.array([m], np.uint16), O.BF16, O.F32)[0]
+        x[r] = np.where(over, x[r] & 0x8000, x[r]).astype(np.uint16)  # smaller than the block max
+    got = gpu_quant(x, False, sr, 99, False, 0)
+    ref = O.nvfp4_quantize(x, False, sr, 99, False, 0)
+    assert_same(got, ref, f"undecided block scales sr={sr}")
+
+
+@pytest.mark.parametrize("scale", [1e-30, 1e-26, 1e-25, 1e35, 1e36])
+@pytest.mark.parametrize("rht,sr", [(False, False), (True, True), (True, False)])
+def test_1x16_tensor_scales_outside_the_fast_range(scale, rht, sr):
+    """Tensor scales below 2^-90 or above 2^110 run every block through the
+    exact divisions and the two-step products; 1e-25 and 1e35 put s_t just
+    inside the edges (s_t is about scale / 84 here)."""
+    x = synth.fill(synth.recipe(81, 0, float(np.float32(scale)), 0.02, 8.0, synth.OUT_SCALE), synth.BF16, 64 * 512,
+                   shape=(64, 512))
+    got = gpu_quant(x, False, sr, 5, rht, 0x5A3C)
+    ref = O.nvfp4_quantize(x, False, sr, 5, rht, 0x5A3C)
+    assert_same(got, ref, f"scale {scale} rht={rht} sr={sr}")
+    assert ref[3] == 0 and ref[2] != 0.0
+
+
+@pytest.mark.parametrize("rht,sr", [(False, False), (False, True), (True, True)])
+def test_1x16_blocks_of_subnormal_values_in_a_normal_tensor(rht, sr):
+    """Blocks whose max is below 2^-120 take the exact path; their codes and
+    scales are mostly zero, a few tiny values survive when the block is all
+    that small and the tensor max is small too."""
+    rows = 48
+    x = synth.fill(synth.recipe(82, 0, 1.0), synth.BF16, rows * 64, shape=(rows, 64))
+    tiny = (synth.fill(synth.recipe(83, 0, 1.0), synth.BF16, rows * 64, shape=(rows, 64)) & 0x807F).astype(np.uint16)
+    x[::2, :32] = tiny[::2, :32]  # subnormals
+    x[1::4] = tiny[1::4] | np.uint16(0x0080)  # the smallest normal binade
+    got = gpu_quant(x, False, sr, 11, rht, 0x1357)
+    ref = O.nvfp4_quantize(x, False, sr, 11, rht, 0x1357)
+    assert_same(got, ref, f"subnormal blocks rht={rht} sr={sr}")
