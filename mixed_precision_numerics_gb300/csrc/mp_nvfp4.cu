@@ -678,14 +678,18 @@ void launch_encode(bool block_2d, const uint16_t* x, int64_t rows, int64_t cols,
     static const int occ = occ_of(k_nvfp4_2d<RHT, SR, DEQ>);
     const int64_t items = (rows / 16) * ((cols + 255) / 256);  // one warp each
     const int64_t ctas = (items + kThreads / 32 - 1) / (kThreads / 32);
-    launch_chained(k_nvfp4_2d<RHT, SR, DEQ>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, rows, cols, mask, seed,
+    // twice as many CTAs as fit at once (measured faster than 1x and 4x)
+    launch_chained(k_nvfp4_2d<RHT, SR, DEQ>, dim3(grid_for(ctas, occ * 2)), dim3(kThreads), 0, s, x, rows, cols, mask, seed,
                    ts, nf, codes, scales, deq);
   } else {
+    // Four times as many CTAs as fit at once: a CTA that finishes early takes
+    // another, so the last wave ends nearly together (measured: 4x beat 1x, 2x,
+    // 8x and 16x; a CTA's table costs 128 divisions, so not more).
     static const int occ = occ_of(k_nvfp4_1x16<RHT, SR, DEQ>);
     const int64_t nblocks = rows * (cols / 16);
     const int64_t ctas = (nblocks + kThreads - 1) / kThreads;
-    launch_chained(k_nvfp4_1x16<RHT, SR, DEQ>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, nblocks, mask, seed,
-                   ts, nf, codes, scales, deq);
+    launch_chained(k_nvfp4_1x16<RHT, SR, DEQ>, dim3(grid_for(ctas, occ * 4)), dim3(kThreads), 0, s, x, nblocks, mask,
+                   seed, ts, nf, codes, scales, deq);
   }
 }
 
