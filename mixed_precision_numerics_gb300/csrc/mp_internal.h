@@ -71,6 +71,15 @@ cudaError_t launch_chained(void (*kernel)(P...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
 }
 
+// Grid for a kernel whose threads each take one batch of work: every CTA it
+// needs, so the block scheduler hands an SM a new CTA as soon as one finishes
+// and the last wave ends nearly together (the kernels keep a grid-stride loop,
+// so a smaller grid stays correct).
+inline int full_grid(int64_t work_ctas) {
+  if (work_ctas < 1) work_ctas = 1;
+  return (int)(work_ctas < INT32_MAX ? work_ctas : INT32_MAX);
+}
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 inline mp_status launch_status() {

@@ -185,19 +185,11 @@ __global__ __launch_bounds__(kThreads) void k_mx_quantize(const void* __restrict
   }
 }
 
-template <typename K>
-int occ_of(K kernel) {
-  int o = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kernel, kThreads, 0) != cudaSuccess || o < 1) o = 1;
-  return o;
-}
-
 template <int XT, int EF>
 mp_status launch(const void* x, int64_t nblk, uint8_t* codes, uint8_t* scales, uint16_t* dq, cudaStream_t s) {
-  static const int occ = occ_of(k_mx_quantize<XT, EF>);
   constexpr int U = unroll_of<XT>();
   const int64_t ctas = (nblk + (int64_t)kThreads * U - 1) / ((int64_t)kThreads * U);
-  launch_chained(k_mx_quantize<XT, EF>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, nblk, codes, scales, dq);
+  launch_chained(k_mx_quantize<XT, EF>, dim3(full_grid(ctas)), dim3(kThreads), 0, s, x, nblk, codes, scales, dq);
   note_launches(1);
   return launch_status();
 }

@@ -779,13 +779,10 @@ MP_API mp_status rht16(const void* x_bf16, int64_t rows, int64_t cols, uint16_t 
   const int64_t ntiles = n / 16;
   const int64_t ctas = (ntiles + kThreads - 1) / kThreads;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
-  if (y_dtype == MP_F32) {
-    static const int occ = occ_of(k_rht16<true>);
-    launch_chained(k_rht16<true>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
-  } else {
-    static const int occ = occ_of(k_rht16<false>);
-    launch_chained(k_rht16<false>, dim3(grid_for(ctas, occ)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
-  }
+  if (y_dtype == MP_F32)
+    launch_chained(k_rht16<true>, dim3(full_grid(ctas)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
+  else
+    launch_chained(k_rht16<false>, dim3(full_grid(ctas)), dim3(kThreads), 0, s, x, ntiles, (uint32_t)sign_mask, y);
   note_launches(1);
   return launch_status();
 }
