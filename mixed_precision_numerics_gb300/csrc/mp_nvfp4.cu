@@ -253,9 +253,10 @@ __device__ __forceinline__ uint32_t nibble_signs(const float (&g)[8]) {
 // [2, 4), [4, 6] the binades of exponent field 1, 2, 3 with the kept mantissa
 // bit at 22.  So bits 22-24 of z are the code rounded toward zero and bits
 // 6-21 are floor(frac * 2^16); (bits(z) + r16 * 2^6) >> 22 is the code after
-// the rule's carry.  The truncating multiply keeps every bit the rule reads
-// (|y| down to 2^-23).  Signs come from y's sign bits.  The adds and shifts
-// here run on the integer pipes, leaving the multiply pipe to Philox.
+// the rule's carry (clamped at 6, whose fraction bits are zero, it stays below
+// 8).  The truncating multiply keeps every bit the rule reads (|y| down to
+// 2^-23).  Signs come from y's sign bits.  No multiply here: the multiply pipe
+// is left to Philox.
 __device__ __forceinline__ uint32_t sr_group(const float (&y)[8], u32x4 R) {
   const uint32_t w[4] = {R.x, R.y, R.z, R.w};
   float a[8];
@@ -268,14 +269,18 @@ __device__ __forceinline__ uint32_t sr_group(const float (&y)[8], u32x4 R) {
     zb[j] = __float_as_uint(z.x);
     zb[j + 1] = __float_as_uint(z.y);
   }
-  uint32_t acc = 0;
+  // Shifted left by 2 the same sum has the code in its top byte: r16 * 2^8 is
+  // a byte permute of the Philox word, and byte permutes gather the top bytes
+  // of the even and the odd elements, one nibble apart.
+  uint32_t u[8];
 #pragma unroll
-  for (int j = 7; j >= 0; --j) {
-    const uint32_t word = w[j >> 1];
-    const uint32_t r6 = (j & 1) ? ((word >> 10) & 0x3FFFC0u) : ((word << 6) & 0x3FFFC0u);  // r16 * 2^6
-    acc = acc * 16u + ((zb[j] + r6) >> 22);
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t r8 = prmt(w[j >> 1], 0u, (j & 1) ? 0x4324u : 0x4104u);  // r16 * 2^8
+    u[j] = (zb[j] << 2) + r8;
   }
-  return acc | (nibble_signs(y) & 0x88888888u);
+  const uint32_t e = prmt(prmt(u[0], u[2], 0x0073u), prmt(u[4], u[6], 0x7300u), 0x7610u);
+  const uint32_t o = prmt(prmt(u[1], u[3], 0x0073u), prmt(u[5], u[7], 0x7300u), 0x7610u);
+  return (e + (o << 4)) | (nibble_signs(y) & 0x88888888u);
 }
 
 // BF16 RNE of value(code) * d for the 16 codes in (lo, hi).
