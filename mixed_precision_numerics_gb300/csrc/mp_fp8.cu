@@ -15,9 +15,9 @@
 //
 // The 2-D tile casts -- the cast with a transposed copy (k_fp8_cast_t_tma)
 // and the fine-grained casts with 1x128 or 128x128 block scales
-// (k_fp8_block_tma) -- read 128 x 128 boxes through 2-D tensor copies into a
-// shared-memory ring that one producer lane keeps full, consumed by groups of
-// eight warps; each wait is bounded and a wait that gives up is counted for
+// (k_fp8_block_tma) -- read 128 x 128 boxes (64 x 128 for 1x128 scales) through
+// 2-D tensor copies into a shared-memory ring that one producer lane keeps full,
+// consumed by groups of eight (four) warps; each wait is bounded and a wait that gives up is counted for
 // mp_wait_failures.
 #include <string.h>
 
@@ -309,7 +309,8 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
 // a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
 // shared-memory stages (six 32 KB stages for 16-bit input, two 64 KB for
-// FP32).  The consumers are kGroups groups of eight warps; group g
+// FP32; for 1x128 scales twice as many stages of half boxes, see BlkGeom).
+// The consumers are kGroups groups of eight (1x128: four) warps; group g
 // takes the CTA's rounds g, g + kGroups, ..., so several blocks are reduced
 // and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
 // elements) of the stage into registers and releases the stage at once, so
@@ -318,7 +319,8 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // group, the partial maxima double-buffered by round; the 1x128 form instead
 // takes each row's maximum by a recursive-halving shuffle exchange and needs
 // no barrier) and cast from registers.  Warp w of a group takes
-// rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15), whole rows,
+// rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15; 1x128: rows
+// 2w + 8k and w + 4k), whole rows,
 // so shared-memory reads cover 512 consecutive bytes per instruction and
 // every store writes whole row segments.  Parts of an edge block outside the
 // tensor arrive as zeros, which leave the amax unchanged, and are not stored.
@@ -336,17 +338,26 @@ __device__ unsigned int g_wait_failures;  // bounded waits that gave up (read by
 // groups would let one group run a fill ahead of the other, see the previous
 // fill's parity and read stale bytes, and its early arrivals would let the
 // producer re-arm a barrier whose phase has not completed.)
-template <int XT>
+//
+// The 1x128 form (ROWS) copies half boxes, 64 rows x 128 columns, to groups of
+// four warps: twice as many work units as 128 x 128 boxes, so the units of a
+// tensor divide more evenly over the persistent CTAs (a [8192 x 4096] tensor:
+// 4096 units, at most 27 per CTA against an average of 26.9, where 2048 boxes
+// gave at most 14 against 13.5).  A thread holds the same kGpt groups either way.
+template <int XT, bool ROWS>
 struct BlkGeom {
   static constexpr int kEs = XT == XF32 ? 4 : 2;                 // input element bytes
   static constexpr int kG = 16 / kEs;                             // elements per 16-byte group
-  static constexpr int kStage = 128 * 128 * kEs;                  // one block
-  static constexpr int kGroups = XT == XF32 ? 2 : 3;              // consumer groups (register budget)
-  static constexpr int kStages = XT == XF32 ? 2 : 6;              // 128 KB or 192 KB of ring
-  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 16-byte groups per consumer thread: 8 or 16
-  static constexpr int kThreads = kGroups * kGroupThreads + 32;   // + the producer warp
+  static constexpr int kBoxRows = ROWS ? 64 : 128;                // rows per copied box (work unit)
+  static constexpr int kGW = ROWS ? 4 : kGroupWarps;              // warps per consumer group
+  static constexpr int kGT = 32 * kGW;                            // threads per consumer group
+  static constexpr int kStage = kBoxRows * 128 * kEs;             // one box
+  static constexpr int kGroups = (XT == XF32 ? 2 : 3) * (ROWS ? 2 : 1);  // consumer groups (register budget)
+  static constexpr int kStages = (XT == XF32 ? 2 : 6) * (ROWS ? 2 : 1);  // 128 KB or 192 KB of ring
+  static constexpr int kGpt = kBoxRows * 128 / kG / kGT;          // 16-byte groups per consumer thread: 8 or 16
+  static constexpr int kThreads = kGroups * kGT + 32;             // + the producer warp
   static constexpr size_t kSmem = (size_t)kStages * kStage + 2 * kStages * sizeof(uint64_t) +
-                                  (size_t)kGroups * 2 * kGroupWarps * sizeof(uint32_t);
+                                  (size_t)kGroups * 2 * kGW * sizeof(uint32_t);
   static_assert(kStages % kGroups == 0, "every ring stage must belong to one consumer group");
   static_assert(kStages * kStage <= kRingBytes, "ring larger than its budget");
 };
@@ -471,32 +482,32 @@ __device__ __forceinline__ uint32_t row_max_scatter(uint32_t (&v)[V], int lane) 
 }
 
 // ROWS = false: one scale per 128 x 128 box (block).  ROWS = true: the box is
-// 128 stacked 1 x 128 tiles, one scale per row of it.
+// 64 stacked 1 x 128 tiles, one scale per row of it.
 template <int XT, bool E5M2, bool ROWS>
-__global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
+__global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
     float* __restrict__ scales) {
   chain_wait();  // the previous kernel in the stream has finished and its writes are visible
   chain_release();
-  using Gm = BlkGeom<XT>;
+  using Gm = BlkGeom<XT, ROWS>;
   constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG;  // groups per row
-  constexpr int kNG = Gm::kGroups;
+  constexpr int kNG = Gm::kGroups, kGW = Gm::kGW, kGT = Gm::kGT, kBR = Gm::kBoxRows;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kS * kSB);
   uint64_t* empty = full + kS;
-  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGroupWarps]
+  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGW]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nbc = (cols + 127) / 128, nb = ((rows + 127) / 128) * nbc;
+  const int64_t nbc = (cols + 127) / 128, nb = ((rows + kBR - 1) / kBR) * nbc;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kGroupWarps);  // the eight warps of the group that reads the stage
+      mbar_init(&empty[i], kGW);  // the warps of the group that reads the stage
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kNG * kGroupWarps) {
+  if (warp == kNG * kGW) {
     // Producer: one lane issues the block copies.
     if (lane != 0) return;
     prefetch_tensor_map(&map);
@@ -510,7 +521,7 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
         break;
       }
       mbar_arrive_expect_tx(&full[sidx], kSB);
-      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128), &full[sidx],
+      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * kBR), &full[sidx],
                   policy);
     }
     if (!ok) {
@@ -524,9 +535,9 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
 
   // Consumers.  A warp whose wait gave up stops reading and storing but keeps
   // meeting its group's named barrier every round, so the group never blocks on it.
-  const int grp = warp / kGroupWarps, gw = warp % kGroupWarps, t = threadIdx.x % kGroupThreads;
-  constexpr int kRowStep = kGroupThreads / kGpr;  // rows between a thread's groups: 16 or 8
-  uint32_t* gred = red + grp * 2 * kGroupWarps;
+  const int grp = warp / kGW, gw = warp % kGW, t = threadIdx.x % kGT;
+  constexpr int kRowStep = kGT / kGpr;  // rows between a thread's groups: 16 or 8 (1x128: 8 or 4)
+  uint32_t* gred = red + grp * 2 * kGW;
   bool ok = true;
   int it = grp, round = 0;
   for (int64_t b = blockIdx.x + (int64_t)grp * gridDim.x; b < nb; b += (int64_t)kNG * gridDim.x, it += kNG, ++round) {
@@ -540,7 +551,7 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
       if (!ok) break;  // no barrier to keep meeting: the warp leaves
       const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
 #pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGT * k];
       uint32_t v[Gm::kGpt];
 #pragma unroll
       for (int k = 0; k < Gm::kGpt; ++k) {
@@ -556,7 +567,7 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
       const float amax = __uint_as_float(row_max_scatter<Gm::kGpt>(v, lane));
       float sc, rm;
       block_scale_of<E5M2>(amax, &sc, &rm);
-      const int64_t bc = b % nbc, row0 = (b / nbc) * 128 + t / kGpr, col = bc * 128 + (t % kGpr) * kG;
+      const int64_t bc = b % nbc, row0 = (b / nbc) * kBR + t / kGpr, col = bc * 128 + (t % kGpr) * kG;
       const int64_t rows_left = rows - row0;
       if ((lane & 1) == 0 && (int64_t)slot * kRowStep < rows_left) scales[(row0 + slot * kRowStep) * nbc + bc] = sc;
       uint8_t* yp = y + row0 * cols + col;
@@ -576,23 +587,23 @@ __global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
     if (ok) {
       const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
 #pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGT * k];
 #pragma unroll
       for (int k = 0; k < Gm::kGpt; ++k) group_max<XT>(raw[k], acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[sidx]);  // the stage's bytes are all in registers
     }
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits(fold_max<XT>(acc)));
-    if (lane == 0) gred[(round & 1) * kGroupWarps + gw] = m;
-    named_barrier(1 + grp, kGroupThreads);
+    if (lane == 0) gred[(round & 1) * kGW + gw] = m;
+    named_barrier(1 + grp, kGT);
     if (!ok) continue;
     uint32_t mb = 0;
 #pragma unroll
-    for (int w = 0; w < kGroupWarps; ++w) mb = max(mb, gred[(round & 1) * kGroupWarps + w]);
+    for (int w = 0; w < kGW; ++w) mb = max(mb, gred[(round & 1) * kGW + w]);
     const float amax = __uint_as_float(mb);
     float sc, r;
     block_scale_of<E5M2>(amax, &sc, &r);
-    const int64_t row0 = (b / nbc) * 128 + t / kGpr, col = (b % nbc) * 128 + (t % kGpr) * kG;
+    const int64_t row0 = (b / nbc) * kBR + t / kGpr, col = (b % nbc) * 128 + (t % kGpr) * kG;
     uint8_t* yp = y + row0 * cols + col;
     const int64_t rows_left = rows - row0;  // this thread's rows k * kRowStep < rows_left exist
     if (col < cols) {
@@ -824,16 +835,19 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
 template <int XT, bool E5M2>
 mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool square, uint8_t* y, float* scales,
                            cudaStream_t s) {
-  using Gm = BlkGeom<XT>;
   CUtensorMap map;
-  if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
-  const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
   if (square) {
+    using Gm = BlkGeom<XT, false>;
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, 128)) return MP_ECUDA;
+    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + 127) / 128);
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, false>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     launch_chained(k_fp8_block_tma<XT, E5M2, false>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
                    rows, cols, y, scales);
   } else {
+    using Gm = BlkGeom<XT, true>;
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, 128)) return MP_ECUDA;
+    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + 127) / 128);
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, true>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     launch_chained(k_fp8_block_tma<XT, E5M2, true>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
