@@ -346,6 +346,19 @@ MP_API mp_status nvfp4_quantize_noalloc(const void* x_bf16, int64_t rows, int64_
                                         uint8_t* block_scales, float* d_tensor_scale,
                                         int32_t* d_nonfinite, void* dequant_bf16, void* stream);
 
+/* e2m1_stochastic_round — the stochastic rounding of nvfp4_quantize
+ * ([NVFP4] §2.2 item 4, "확률적 반올림") on values the caller supplies, with
+ * random bits the caller supplies: for i < n, the E2M1 code of y[i] rounded
+ * away from zero iff floor(frac * 2^16) + r16[i] >= 2^16, frac the position of
+ * |y[i]| between its grid neighbours (0, 0.5, 1, 1.5, 2, 3, 4, 6); magnitudes
+ * from 6 up (infinities included) and NaN give 6; the sign bit is kept (-0
+ * gives 0x8).  y: FP32 [n], r16: uint16 [n], codes: [(n + 1) / 2] bytes,
+ * element 2j in the low nibble of byte j (the high nibble of the last byte is
+ * 0 when n is odd); all device pointers, 16-byte aligned (MP_EALIGN), n >= 0
+ * (MP_EINVAL).  One kernel launch; the caller owns every buffer. */
+MP_API mp_status e2m1_stochastic_round(const float* y, const uint16_t* r16, int64_t n, uint8_t* codes,
+                                       void* stream);
+
 /* rht16 — the 16-point random Hadamard transform ([NVFP4] §2.2 item 2):
  * for every 16 contiguous elements t of each row of BF16 x [rows, cols],
  * y_t = 1/4 * H16 * diag(s) * x_t, H16 the Sylvester Hadamard matrix

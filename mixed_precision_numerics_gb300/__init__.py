@@ -108,6 +108,7 @@ def _load() -> ctypes.CDLL:
         "nvfp4_workspace_size": (S, []),
         "nvfp4_quantize": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P, S, P]),
         "rht16": (I32, [P, I64, I64, U16, P, I32, P]),
+        "e2m1_stochastic_round": (I32, [P, P, I64, P, P]),
         "nvfp4_noalloc_scratch_bytes": (S, []),
         "nvfp4_quantize_noalloc": (I32, [P, I64, I64, I32, I32, U64, I32, U16, P, P, P, P, P, P]),
         "mx_quantize": (I32, [P, I32, I64, I64, I32, P, P, P, P]),
@@ -439,6 +440,16 @@ def rht16(x, y, sign_mask: int, stream=None) -> None:
     _check("rht16", lib.rht16(_ptr(x), rows, cols, sign_mask & 0xFFFF, _ptr(y), _dtype_code(y), _stream(stream)))
 
 
+def e2m1_stochastic_round(y, r16, codes, stream=None) -> None:
+    """y: FP32 [n]; r16: 16-bit [n] random values (int16 or uint16 storage);
+    codes: uint8 [(n + 1) // 2], element 2j in the low nibble of byte j."""
+    n = y.numel()
+    _dev(y, "y", 4 * n)
+    _dev(r16, "r16", 2 * n, like=y)
+    _dev(codes, "codes", (n + 1) // 2, like=y)
+    _check("e2m1_stochastic_round", lib.e2m1_stochastic_round(_ptr(y), _ptr(r16), n, _ptr(codes), _stream(stream)))
+
+
 def mx_quantize(x, codes, scales, elem_dtype: int = MP_E2M1, dequant=None, stream=None) -> None:
     """x: [rows, cols], cols % 32 == 0; codes: rows*cols bytes (FP8, FP6) or
     rows*cols/2 (E2M1); scales: uint8 [rows, cols/32] (UE8M0)."""
@@ -458,7 +469,7 @@ __all__ = [
     "MP_F32", "MP_F16", "MP_BF16", "MP_E4M3", "MP_E5M2", "MP_E2M1", "MP_E2M3", "MP_E3M2", "mx_quantize",
     "mp_adamw_step", "mp_adamw_check", "mp_adamw_apply", "mp_adamw_workspace_size", "loss_scale_update",
     "fp8_cast_transpose_delayed", "fp8_cast_delayed_count", "fp8_quantize_blockwise", "MP_AMAX_HISTORY_MAX", "MP_AMAX_MOST_RECENT",
-    "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16",
+    "nvfp4_quantize_noalloc", "fp8_cast_delayed", "nvfp4_quantize", "rht16", "e2m1_stochastic_round",
     "nvfp4_workspace_size", "mp_status_str", "mp_launch_count", "mp_wait_failures",
     "new_scaler_state", "new_fp8_meta", "new_nvfp4_workspace", "read_scaler_state", "read_fp8_meta",
     "make_param_array",

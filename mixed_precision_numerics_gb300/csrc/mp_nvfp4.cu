@@ -426,7 +426,7 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_1x16(const uint16_t* __restr
 // Encode 8 values of x' (half a 1x16 tile, flat index `flat` a multiple of 8)
 // with block reciprocal r; returns 8 codes, element j in nibble j.  Stochastic
 // rounding takes the 8 random halves of the one Philox call for counter
-// flat / 8, as encode16 does for each half of its tile.
+// flat / 8, as the 1x16 encode does for each half of its tile.
 template <bool SR>
 __device__ __forceinline__ uint32_t encode8(const float (&v)[8], float r, uint64_t flat, uint32_t k0, uint32_t k1) {
   uint32_t q = 0;
@@ -584,6 +584,35 @@ __global__ __launch_bounds__(kThreads) void k_nvfp4_2d(const uint16_t* __restric
   }
 }
 
+// Stochastic E2M1 codes of y with caller-supplied random bits (element i
+// takes r16[i]), two elements a thread through the same conversion as the
+// encode; codes two per byte, element 2j in the low nibble.  A NaN takes code
+// 7 with its sign bit, as the rule's comparison (|NaN| < 6 is false) gives,
+// where the conversion alone would give +6.
+__global__ __launch_bounds__(kThreads) void k_e2m1_sr(const float* __restrict__ y, const uint16_t* __restrict__ r16,
+                                                      int64_t n, uint8_t* __restrict__ codes) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
+  const int64_t npairs = (n + 1) / 2, stride = (int64_t)gridDim.x * kThreads;
+  for (int64_t j = (int64_t)blockIdx.x * kThreads + threadIdx.x; j < npairs; j += stride) {
+    const int64_t i = 2 * j;
+    const float lo = y[i];
+    const uint32_t rlo = r16[i];
+    float hi = 0.0f;
+    uint32_t rhi = 0u;
+    if (i + 1 < n) {
+      hi = y[i + 1];
+      rhi = r16[i + 1];
+    }
+    // rbits bytes 2:0 = rlo (lane e, lo), bytes 3:1 = rhi (lane b, hi)
+    const uint32_t d = cvt_rs_e2m1_pair(lo, hi, prmt(rlo | (rhi << 16), 0u, 0x3120u));
+    uint32_t q = (d | (d >> 4)) & 0xFFu;
+    if (lo != lo) q = (q & 0xF0u) | 7u | ((__float_as_uint(lo) >> 28) & 8u);
+    if (hi != hi) q = (q & 0x0Fu) | 0x70u | ((__float_as_uint(hi) >> 24) & 0x80u);
+    codes[j] = (uint8_t)q;
+  }
+}
+
 template <bool F32OUT>
 __global__ __launch_bounds__(kThreads) void k_rht16(const uint16_t* __restrict__ x, int64_t ntiles, uint32_t mask,
                                                     void* __restrict__ y) {
@@ -736,6 +765,20 @@ MP_API mp_status nvfp4_quantize(const void* x_bf16, int64_t rows, int64_t cols, 
   else
     dispatch_deq<false, false>(deq, b2, x, rows, cols, mask, seed, d_tensor_scale, d_nonfinite, codes, block_scales, dq, s);
   note_launches(2);
+  return launch_status();
+}
+
+MP_API mp_status e2m1_stochastic_round(const float* y, const uint16_t* r16, int64_t n, uint8_t* codes,
+                                       void* stream) {
+  using namespace mp;
+  if (n < 0) return MP_EINVAL;
+  if (n > 0 && (!y || !r16 || !codes)) return MP_EINVAL;
+  if (n > 0 && (!aligned16(y) || !aligned16(r16) || !aligned16(codes))) return MP_EALIGN;
+  if (n == 0) return MP_OK;
+  const int64_t ctas = ((n + 1) / 2 + kThreads - 1) / kThreads;
+  launch_chained(k_e2m1_sr, dim3(full_grid(ctas)), dim3(kThreads), 0, static_cast<cudaStream_t>(stream), y, r16, n,
+                 codes);
+  note_launches(1);
   return launch_status();
 }
 

@@ -106,6 +106,7 @@ def lib() -> ctypes.CDLL:
             "orc_philox4x32_10": (None, [P, P, P]),
             "orc_sr_bits": (U32, [U64, U64]),
             "orc_e2m1_sr_array": (None, [P, I64, U64, U64, P]),
+            "orc_e2m1_sr_bits_array": (None, [P, P, I64, P]),
             "orc_rht16_tile": (None, [P, U16, P]),
             "orc_rht16": (ctypes.c_int, [P, I64, I64, U16, P, ctypes.c_int]),
             "orc_nonfinite_any": (ctypes.c_int, [P, ctypes.c_int, I64]),
@@ -187,6 +188,16 @@ def e2m1_sr_array(y: np.ndarray, seed: int, i0: int = 0) -> np.ndarray:
     y = np.ascontiguousarray(y, dtype=np.float32)
     out = np.empty(y.size, dtype=np.uint8)
     lib().orc_e2m1_sr_array(_p(y), y.size, seed, i0, _p(out))
+    return out
+
+
+def e2m1_sr_with_bits(y: np.ndarray, r16: np.ndarray) -> np.ndarray:
+    """Stochastic E2M1 code of each y[k] with the 16 random bits r16[k] (one code per byte)."""
+    y = np.ascontiguousarray(y, dtype=np.float32).reshape(-1)
+    r16 = np.ascontiguousarray(r16, dtype=np.uint16).reshape(-1)
+    assert y.size == r16.size
+    out = np.empty(y.size, dtype=np.uint8)
+    lib().orc_e2m1_sr_bits_array(_p(y), _p(r16), y.size, _p(out))
     return out
 
 

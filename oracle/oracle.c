@@ -266,6 +266,10 @@ void orc_e2m1_sr_array(const float* y, int64_t n, uint64_t seed, uint64_t i0, ui
   for (int64_t k = 0; k < n; ++k) out[k] = orc_f32_to_e2m1_sr(y[k], orc_sr_bits(seed, i0 + (uint64_t)k));
 }
 
+void orc_e2m1_sr_bits_array(const float* y, const uint16_t* r16, int64_t n, uint8_t* out) {
+  for (int64_t k = 0; k < n; ++k) out[k] = orc_f32_to_e2m1_sr(y[k], r16[k]);
+}
+
 /* ---------------------------------------------------------------------------
  * [NVFP4] §2.2 item 2 "랜덤 하다마드 변환": a 16x16 random Hadamard transform
  * spreads outliers before FP4 quantisation.  Reading R16: H16 is the

@@ -76,6 +76,8 @@ void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
 uint32_t orc_sr_bits(uint64_t seed, uint64_t i);
 /* out[k] = stochastic E2M1 code of y[k] with the bits of index i0 + k. */
 void orc_e2m1_sr_array(const float* y, int64_t n, uint64_t seed, uint64_t i0, uint8_t* out);
+/* out[k] = stochastic E2M1 code of y[k] with the random bits r16[k]. */
+void orc_e2m1_sr_bits_array(const float* y, const uint16_t* r16, int64_t n, uint8_t* out);
 
 /* ---- 16-point random Hadamard transform ([NVFP4] §2.2 item 2) -------------- */
 /* out = 1/4 * H16 * diag(s) * in, H16 Sylvester, s_j = -1 iff bit j of mask. */

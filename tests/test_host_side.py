@@ -92,6 +92,11 @@ def test_argument_validation_without_gpu(M):
     t = L.fp8_cast_transpose_delayed
     assert t(16, M.MP_BF16, 16, 24, 16, 16, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_ESHAPE
     assert t(16, M.MP_BF16, 16, 32, 16, 8, M.MP_E4M3, 16, 16, 4, 1.0, 0, None) == M.MP_EALIGN
+    e = L.e2m1_stochastic_round
+    assert e(16, 16, -1, 16, None) == M.MP_EINVAL
+    assert e(16, None, 4, 16, None) == M.MP_EINVAL
+    assert e(16, 16, 4, 24, None) == M.MP_EALIGN
+    assert e(None, None, 0, None, None) == M.MP_OK
     q = L.nvfp4_quantize
     assert q(16, 2, 24, 0, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
     assert q(16, 8, 32, 1, 0, 0, 0, 0, 16, 16, 16, 16, None, 16, 256, None) == M.MP_ESHAPE
