@@ -853,9 +853,10 @@ def main():
     if "nvfp4_grad_rht_1x16_sr" in kernels:
         kernels["nvfp4_grad_rht_1x16_sr"]["bound"] = "issue"
         kernels["nvfp4_grad_rht_1x16_sr"]["note"] = (
-            "the encode pass runs about 22.7 instructions per element (Philox4x32-10 at one call per 8 elements, "
-            "the Hadamard butterfly, software stochastic rounding); ncu shows issue slots 66 % busy, the integer and "
-            "FMA-heavy pipes 66 % and 64 % busy and DRAM about 30 %, so its HBM fraction is not its limit")
+            "the encode pass runs about 17.2 instructions per element (Philox4x32-10 at one call per 8 elements, "
+            "whose wide multiplies hold the FMA-heavy pipe, the Hadamard butterfly, stochastic rounding by the "
+            "hardware conversion two elements at a time); ncu shows issue slots 65 % busy, the FMA-heavy and "
+            "integer pipes 64 % and 58 % busy and DRAM about 35 %, so its HBM fraction is not its limit")
     if "fp8_act_e4m3" in kernels:
         kernels["fp8_act_e4m3"]["note"] = ("runs right after the update kernel and pays for the dirty L2 lines "
                                            "that kernel leaves; graph_isolated_* is the same call alone")
