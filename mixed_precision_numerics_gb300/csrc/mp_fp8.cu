@@ -15,7 +15,7 @@
 //
 // The 2-D tile casts -- the cast with a transposed copy (k_fp8_cast_t_tma)
 // and the fine-grained casts with 1x128 or 128x128 block scales
-// (k_fp8_block_tma) -- read 128 x 128 boxes (64 x 128 for 1x128 scales) through
+// (k_fp8_block_tma) -- read 128 x 128 boxes (32 x 256 for 1x128 scales) through
 // 2-D tensor copies into a shared-memory ring that one producer lane keeps full,
 // consumed by groups of eight (four) warps; each wait is bounded and a wait that gives up is counted for
 // mp_wait_failures.
@@ -309,7 +309,7 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
 // a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
 // shared-memory stages (six 32 KB stages for 16-bit input, two 64 KB for
-// FP32; for 1x128 scales twice as many stages of half boxes, see BlkGeom).
+// FP32; for 1x128 scales twice as many stages of 32 x 256 boxes, see BlkGeom).
 // The consumers are kGroups groups of eight (1x128: four) warps; group g
 // takes the CTA's rounds g, g + kGroups, ..., so several blocks are reduced
 // and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
@@ -320,7 +320,8 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // takes each row's maximum by a recursive-halving shuffle exchange and needs
 // no barrier) and cast from registers.  Warp w of a group takes
 // rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15; 1x128: rows
-// 2w + 8k and w + 4k), whole rows,
+// w + 4k, k = 0..7, both 128-column tiles, or for FP32 tile w mod 2 of rows
+// w / 2 + 2k, k = 0..15), whole row segments,
 // so shared-memory reads cover 512 consecutive bytes per instruction and
 // every store writes whole row segments.  Parts of an edge block outside the
 // tensor arrive as zeros, which leave the amax unchanged, and are not stored.
@@ -339,22 +340,26 @@ __device__ unsigned int g_wait_failures;  // bounded waits that gave up (read by
 // fill's parity and read stale bytes, and its early arrivals would let the
 // producer re-arm a barrier whose phase has not completed.)
 //
-// The 1x128 form (ROWS) copies half boxes, 64 rows x 128 columns, to groups of
-// four warps: twice as many work units as 128 x 128 boxes, so the units of a
-// tensor divide more evenly over the persistent CTAs (a [8192 x 4096] tensor:
-// 4096 units, at most 27 per CTA against an average of 26.9, where 2048 boxes
-// gave at most 14 against 13.5).  A thread holds the same kGpt groups either way.
+// The 1x128 form (ROWS) copies boxes of 32 rows x 256 columns (two 1x128 tiles
+// of each row) to groups of four warps.  Against 128 x 128 boxes: twice as many
+// work units, so the units of a tensor divide more evenly over the persistent
+// CTAs (a [8192 x 4096] tensor: 4096 units, at most 27 per CTA against an
+// average of 26.9, where 2048 boxes gave at most 14 against 13.5), and each
+// copied row segment is 512 contiguous bytes instead of 256, which DRAM serves
+// faster (measured: 128 x 128 boxes 19.9 us, 64 x 128 19.6-19.8, 32 x 256 19.3).
+// A thread holds the same kGpt groups either way; a 1x128 tile is 16 lanes.
 template <int XT, bool ROWS>
 struct BlkGeom {
   static constexpr int kEs = XT == XF32 ? 4 : 2;                 // input element bytes
   static constexpr int kG = 16 / kEs;                             // elements per 16-byte group
-  static constexpr int kBoxRows = ROWS ? 64 : 128;                // rows per copied box (work unit)
+  static constexpr int kBoxRows = ROWS ? 32 : 128;                // rows per copied box (work unit)
+  static constexpr int kBoxCols = ROWS ? 256 : 128;               // columns per copied box
   static constexpr int kGW = ROWS ? 4 : kGroupWarps;              // warps per consumer group
   static constexpr int kGT = 32 * kGW;                            // threads per consumer group
-  static constexpr int kStage = kBoxRows * 128 * kEs;             // one box
+  static constexpr int kStage = kBoxRows * kBoxCols * kEs;        // one box
   static constexpr int kGroups = (XT == XF32 ? 2 : 3) * (ROWS ? 2 : 1);  // consumer groups (register budget)
   static constexpr int kStages = (XT == XF32 ? 2 : 6) * (ROWS ? 2 : 1);  // 128 KB or 192 KB of ring
-  static constexpr int kGpt = kBoxRows * 128 / kG / kGT;          // 16-byte groups per consumer thread: 8 or 16
+  static constexpr int kGpt = kBoxRows * kBoxCols / kG / kGT;     // 16-byte groups per consumer thread: 8 or 16
   static constexpr int kThreads = kGroups * kGT + 32;             // + the producer warp
   static constexpr size_t kSmem = (size_t)kStages * kStage + 2 * kStages * sizeof(uint64_t) +
                                   (size_t)kGroups * 2 * kGW * sizeof(uint32_t);
@@ -482,7 +487,7 @@ __device__ __forceinline__ uint32_t row_max_scatter(uint32_t (&v)[V], int lane) 
 }
 
 // ROWS = false: one scale per 128 x 128 box (block).  ROWS = true: the box is
-// 64 stacked 1 x 128 tiles, one scale per row of it.
+// 32 rows of two 1 x 128 tiles each, one scale per tile.
 template <int XT, bool E5M2, bool ROWS>
 __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
@@ -491,13 +496,14 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
   chain_release();
   using Gm = BlkGeom<XT, ROWS>;
   constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG;  // groups per row
-  constexpr int kNG = Gm::kGroups, kGW = Gm::kGW, kGT = Gm::kGT, kBR = Gm::kBoxRows;
+  constexpr int kNG = Gm::kGroups, kGW = Gm::kGW, kGT = Gm::kGT, kBR = Gm::kBoxRows, kBC = Gm::kBoxCols;
+  constexpr int kGprB = kBC / kG;  // groups per box row
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kS * kSB);
   uint64_t* empty = full + kS;
   uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGW]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nbc = (cols + 127) / 128, nb = ((rows + kBR - 1) / kBR) * nbc;
+  const int64_t nbc = (cols + 127) / 128, nbu = (cols + kBC - 1) / kBC, nb = ((rows + kBR - 1) / kBR) * nbu;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kS; ++i) {
       mbar_init(&full[i], 1);
@@ -521,7 +527,7 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
         break;
       }
       mbar_arrive_expect_tx(&full[sidx], kSB);
-      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * kBR), &full[sidx],
+      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbu) * kBC), (int32_t)((b / nbu) * kBR), &full[sidx],
                   policy);
     }
     if (!ok) {
@@ -536,7 +542,7 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
   // Consumers.  A warp whose wait gave up stops reading and storing but keeps
   // meeting its group's named barrier every round, so the group never blocks on it.
   const int grp = warp / kGW, gw = warp % kGW, t = threadIdx.x % kGT;
-  constexpr int kRowStep = kGT / kGpr;  // rows between a thread's groups: 16 or 8 (1x128: 8 or 4)
+  constexpr int kRowStep = kGT / kGprB;  // rows between a thread's groups
   uint32_t* gred = red + grp * 2 * kGW;
   bool ok = true;
   int it = grp, round = 0;
@@ -567,9 +573,10 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
       const float amax = __uint_as_float(row_max_scatter<Gm::kGpt>(v, lane));
       float sc, rm;
       block_scale_of<E5M2>(amax, &sc, &rm);
-      const int64_t bc = b % nbc, row0 = (b / nbc) * kBR + t / kGpr, col = bc * 128 + (t % kGpr) * kG;
+      const int64_t row0 = (b / nbu) * kBR + t / kGprB, col = (b % nbu) * kBC + (t % kGprB) * kG, bc = col / 128;
       const int64_t rows_left = rows - row0;
-      if ((lane & 1) == 0 && (int64_t)slot * kRowStep < rows_left) scales[(row0 + slot * kRowStep) * nbc + bc] = sc;
+      if ((lane & 1) == 0 && bc * 128 < cols && (int64_t)slot * kRowStep < rows_left)
+        scales[(row0 + slot * kRowStep) * nbc + bc] = sc;
       uint8_t* yp = y + row0 * cols + col;
 #pragma unroll
       for (int k = 0; k < Gm::kGpt; ++k) {
@@ -603,7 +610,7 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
     const float amax = __uint_as_float(mb);
     float sc, r;
     block_scale_of<E5M2>(amax, &sc, &r);
-    const int64_t row0 = (b / nbc) * kBR + t / kGpr, col = (b % nbc) * 128 + (t % kGpr) * kG;
+    const int64_t row0 = (b / nbu) * kBR + t / kGpr, col = (b % nbu) * 128 + (t % kGpr) * kG;
     uint8_t* yp = y + row0 * cols + col;
     const int64_t rows_left = rows - row0;  // this thread's rows k * kRowStep < rows_left exist
     if (col < cols) {
@@ -838,16 +845,16 @@ mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool squar
   CUtensorMap map;
   if (square) {
     using Gm = BlkGeom<XT, false>;
-    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, 128)) return MP_ECUDA;
-    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + 127) / 128);
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, Gm::kBoxCols)) return MP_ECUDA;
+    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + Gm::kBoxCols - 1) / Gm::kBoxCols);
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, false>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     launch_chained(k_fp8_block_tma<XT, E5M2, false>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
                    rows, cols, y, scales);
   } else {
     using Gm = BlkGeom<XT, true>;
-    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, 128)) return MP_ECUDA;
-    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + 127) / 128);
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, Gm::kBoxCols)) return MP_ECUDA;
+    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + Gm::kBoxCols - 1) / Gm::kBoxCols);
     static std::atomic<uint64_t> smem_done{0};
     if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, true>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
     launch_chained(k_fp8_block_tma<XT, E5M2, true>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
