@@ -14,11 +14,12 @@
 // ring slot and derives the next scale from the two maxima.
 //
 // The 2-D tile casts -- the cast with a transposed copy (k_fp8_cast_t_tma)
-// and the fine-grained casts with 1x128 or 128x128 block scales
-// (k_fp8_block_tma) -- read 128 x 128 boxes (32 x 256 for 1x128 scales) through
-// 2-D tensor copies into a shared-memory ring that one producer lane keeps full,
-// consumed by groups of eight (four) warps; each wait is bounded and a wait that gives up is counted for
-// mp_wait_failures.
+// and the fine-grained cast with 128x128 block scales (k_fp8_block_tma) --
+// read 128 x 128 boxes through 2-D tensor copies into a shared-memory ring
+// that one producer lane keeps full, consumed by groups of eight warps; each
+// wait is bounded and a wait that gives up is counted for mp_wait_failures.
+// The cast with 1x128 tile scales (k_fp8_rows128) reads into registers, four
+// lanes per tile, with every CTA the tensor needs launched at once.
 #include <string.h>
 
 #include "mp_chain.cuh"
@@ -309,19 +310,15 @@ __device__ __forceinline__ void block_scale_of(float amax, float* s, float* r) {
 // 128 x 128 blocks through the tensor-copy engine.  One persistent CTA per SM:
 // a producer warp (one lane) issues one 2-D TMA copy per block into a ring of
 // shared-memory stages (six 32 KB stages for 16-bit input, two 64 KB for
-// FP32; for 1x128 scales twice as many stages of 32 x 256 boxes, see BlkGeom).
-// The consumers are kGroups groups of eight (1x128: four) warps; group g
+// FP32).  The consumers are kGroups groups of eight warps; group g
 // takes the CTA's rounds g, g + kGroups, ..., so several blocks are reduced
 // and cast at once.  A consumer thread reads its 16-byte groups (8 or 4
 // elements) of the stage into registers and releases the stage at once, so
 // the next copy starts while the block is reduced (four independent maxima,
 // packed for 16-bit input, a warp reduction, then one named barrier per
-// group, the partial maxima double-buffered by round; the 1x128 form instead
-// takes each row's maximum by a recursive-halving shuffle exchange and needs
-// no barrier) and cast from registers.  Warp w of a group takes
-// rows 2w + 16k, k = 0..7 (16-bit; FP32 rows w + 8k, k = 0..15; 1x128: rows
-// w + 4k, k = 0..7, both 128-column tiles, or for FP32 tile w mod 2 of rows
-// w / 2 + 2k, k = 0..15), whole row segments,
+// group, the partial maxima double-buffered by round) and cast from
+// registers.  Warp w of a group takes rows 2w + 16k, k = 0..7 (16-bit; FP32
+// rows w + 8k, k = 0..15), whole row segments,
 // so shared-memory reads cover 512 consecutive bytes per instruction and
 // every store writes whole row segments.  Parts of an edge block outside the
 // tensor arrive as zeros, which leave the amax unchanged, and are not stored.
@@ -339,30 +336,17 @@ __device__ unsigned int g_wait_failures;  // bounded waits that gave up (read by
 // groups would let one group run a fill ahead of the other, see the previous
 // fill's parity and read stale bytes, and its early arrivals would let the
 // producer re-arm a barrier whose phase has not completed.)
-//
-// The 1x128 form (ROWS) copies boxes of 32 rows x 256 columns (two 1x128 tiles
-// of each row) to groups of four warps.  Against 128 x 128 boxes: twice as many
-// work units, so the units of a tensor divide more evenly over the persistent
-// CTAs (a [8192 x 4096] tensor: 4096 units, at most 27 per CTA against an
-// average of 26.9, where 2048 boxes gave at most 14 against 13.5), and each
-// copied row segment is 512 contiguous bytes instead of 256, which DRAM serves
-// faster (measured: 128 x 128 boxes 19.9 us, 64 x 128 19.6-19.8, 32 x 256 19.3).
-// A thread holds the same kGpt groups either way; a 1x128 tile is 16 lanes.
-template <int XT, bool ROWS>
+template <int XT>
 struct BlkGeom {
   static constexpr int kEs = XT == XF32 ? 4 : 2;                 // input element bytes
   static constexpr int kG = 16 / kEs;                             // elements per 16-byte group
-  static constexpr int kBoxRows = ROWS ? 32 : 128;                // rows per copied box (work unit)
-  static constexpr int kBoxCols = ROWS ? 256 : 128;               // columns per copied box
-  static constexpr int kGW = ROWS ? 4 : kGroupWarps;              // warps per consumer group
-  static constexpr int kGT = 32 * kGW;                            // threads per consumer group
-  static constexpr int kStage = kBoxRows * kBoxCols * kEs;        // one box
-  static constexpr int kGroups = (XT == XF32 ? 2 : 3) * (ROWS ? 2 : 1);  // consumer groups (register budget)
-  static constexpr int kStages = (XT == XF32 ? 2 : 6) * (ROWS ? 2 : 1);  // 128 KB or 192 KB of ring
-  static constexpr int kGpt = kBoxRows * kBoxCols / kG / kGT;     // 16-byte groups per consumer thread: 8 or 16
-  static constexpr int kThreads = kGroups * kGT + 32;             // + the producer warp
+  static constexpr int kStage = 128 * 128 * kEs;                  // one block
+  static constexpr int kGroups = XT == XF32 ? 2 : 3;              // consumer groups (register budget)
+  static constexpr int kStages = XT == XF32 ? 2 : 6;              // 128 KB or 192 KB of ring
+  static constexpr int kGpt = 128 * 128 / kG / kGroupThreads;     // 16-byte groups per consumer thread: 8 or 16
+  static constexpr int kThreads = kGroups * kGroupThreads + 32;   // + the producer warp
   static constexpr size_t kSmem = (size_t)kStages * kStage + 2 * kStages * sizeof(uint64_t) +
-                                  (size_t)kGroups * 2 * kGW * sizeof(uint32_t);
+                                  (size_t)kGroups * 2 * kGroupWarps * sizeof(uint32_t);
   static_assert(kStages % kGroups == 0, "every ring stage must belong to one consumer group");
   static_assert(kStages * kStage <= kRingBytes, "ring larger than its budget");
 };
@@ -465,55 +449,32 @@ __device__ __forceinline__ uint2 cast_group_finite(const uint4 q, float r) {
   return make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
 }
 
-// Row maxima of a thread's kGpt groups, one per row slot k, reduced over the
-// L = 2 kGpt lanes that share those rows by recursive halving: at the step
-// with n values left, the lane keeps the upper or lower half (by lane bit n)
-// and takes the max with the half its partner at distance n sent, so after
-// log2(kGpt) steps it holds slot ((lane & (2 kGpt - 2)) >> 1), and a last
-// exchange at distance 1 completes it: 2 kGpt - 1 shuffles in all, instead of
-// kGpt log2(L).
-template <int V>
-__device__ __forceinline__ uint32_t row_max_scatter(uint32_t (&v)[V], int lane) {
-#pragma unroll
-  for (int n = V; n >= 2; n >>= 1) {
-    const bool up = (lane & n) != 0;
-#pragma unroll
-    for (int j = 0; j < n / 2; ++j) {
-      const uint32_t keep = up ? v[j + n / 2] : v[j], send = up ? v[j] : v[j + n / 2];
-      v[j] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, n));
-    }
-  }
-  return max(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], 1));
-}
-
-// ROWS = false: one scale per 128 x 128 box (block).  ROWS = true: the box is
-// 32 rows of two 1 x 128 tiles each, one scale per tile.
-template <int XT, bool E5M2, bool ROWS>
-__global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tma(
+// One scale per 128 x 128 box (block).
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(BlkGeom<XT>::kThreads, 1) void k_fp8_block_tma(
     const __grid_constant__ CUtensorMap map, int64_t rows, int64_t cols, uint8_t* __restrict__ y,
     float* __restrict__ scales) {
   chain_wait();  // the previous kernel in the stream has finished and its writes are visible
   chain_release();
-  using Gm = BlkGeom<XT, ROWS>;
+  using Gm = BlkGeom<XT>;
   constexpr int kS = Gm::kStages, kSB = Gm::kStage, kG = Gm::kG, kGpr = 128 / kG;  // groups per row
-  constexpr int kNG = Gm::kGroups, kGW = Gm::kGW, kGT = Gm::kGT, kBR = Gm::kBoxRows, kBC = Gm::kBoxCols;
-  constexpr int kGprB = kBC / kG;  // groups per box row
+  constexpr int kNG = Gm::kGroups;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kS * kSB);
   uint64_t* empty = full + kS;
-  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGW]
+  uint32_t* red = reinterpret_cast<uint32_t*>(empty + kS);  // [kGroups][2][kGroupWarps]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t nbc = (cols + 127) / 128, nbu = (cols + kBC - 1) / kBC, nb = ((rows + kBR - 1) / kBR) * nbu;
+  const int64_t nbc = (cols + 127) / 128, nb = ((rows + 127) / 128) * nbc;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kS; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kGW);  // the warps of the group that reads the stage
+      mbar_init(&empty[i], kGroupWarps);  // the eight warps of the group that reads the stage
     }
     fence_mbar_init();
   }
   __syncthreads();
 
-  if (warp == kNG * kGW) {
+  if (warp == kNG * kGroupWarps) {
     // Producer: one lane issues the block copies.
     if (lane != 0) return;
     prefetch_tensor_map(&map);
@@ -527,7 +488,7 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
         break;
       }
       mbar_arrive_expect_tx(&full[sidx], kSB);
-      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbu) * kBC), (int32_t)((b / nbu) * kBR), &full[sidx],
+      tma_load_2d(smem + sidx * kSB, &map, (int32_t)((b % nbc) * 128), (int32_t)((b / nbc) * 128), &full[sidx],
                   policy);
     }
     if (!ok) {
@@ -541,9 +502,9 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
 
   // Consumers.  A warp whose wait gave up stops reading and storing but keeps
   // meeting its group's named barrier every round, so the group never blocks on it.
-  const int grp = warp / kGW, gw = warp % kGW, t = threadIdx.x % kGT;
-  constexpr int kRowStep = kGT / kGprB;  // rows between a thread's groups
-  uint32_t* gred = red + grp * 2 * kGW;
+  const int grp = warp / kGroupWarps, gw = warp % kGroupWarps, t = threadIdx.x % kGroupThreads;
+  constexpr int kRowStep = kGroupThreads / kGpr;  // rows between a thread's groups: 16 or 8
+  uint32_t* gred = red + grp * 2 * kGroupWarps;
   bool ok = true;
   int it = grp, round = 0;
   for (int64_t b = blockIdx.x + (int64_t)grp * gridDim.x; b < nb; b += (int64_t)kNG * gridDim.x, it += kNG, ++round) {
@@ -553,64 +514,27 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
       if (!ok && lane == 0) atomicAdd(&g_wait_failures, 1u);
     }
     uint4 raw[Gm::kGpt];
-    if constexpr (ROWS) {
-      if (!ok) break;  // no barrier to keep meeting: the warp leaves
-      const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
-#pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGT * k];
-      uint32_t v[Gm::kGpt];
-#pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) {
-        uint32_t acc[4] = {0u, 0u, 0u, 0u};
-        group_max<XT>(raw[k], acc);
-        v[k] = amax_bits(fold_max<XT>(acc));
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[sidx]);  // the stage's bytes are all in registers
-      // This lane's row slot, its amax, scale and multiplier; then every
-      // slot's multiplier from the even lane that holds it.
-      const int slot = (lane & (2 * Gm::kGpt - 2)) >> 1, base = lane & ~(kGpr - 1);
-      const float amax = __uint_as_float(row_max_scatter<Gm::kGpt>(v, lane));
-      float sc, rm;
-      block_scale_of<E5M2>(amax, &sc, &rm);
-      const int64_t row0 = (b / nbu) * kBR + t / kGprB, col = (b % nbu) * kBC + (t % kGprB) * kG, bc = col / 128;
-      const int64_t rows_left = rows - row0;
-      if ((lane & 1) == 0 && bc * 128 < cols && (int64_t)slot * kRowStep < rows_left)
-        scales[(row0 + slot * kRowStep) * nbc + bc] = sc;
-      uint8_t* yp = y + row0 * cols + col;
-#pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) {
-        const float r = __shfl_sync(0xFFFFFFFFu, rm, base | (k << 1));
-        if (col >= cols || k * kRowStep >= rows_left) continue;
-        const uint2 o = r > 0.0f ? cast_group_finite<XT, E5M2>(raw[k], r) : cast_group<XT, E5M2>(raw[k], r);
-        if constexpr (XT == XF32)
-          __stcs(reinterpret_cast<uint32_t*>(yp + (int64_t)k * kRowStep * cols), o.x);
-        else
-          __stcs(reinterpret_cast<uint2*>(yp + (int64_t)k * kRowStep * cols), o);
-      }
-      continue;
-    }
     uint32_t acc[4] = {0u, 0u, 0u, 0u};
     if (ok) {
       const uint4* st = reinterpret_cast<const uint4*>(smem + sidx * kSB);
 #pragma unroll
-      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGT * k];
+      for (int k = 0; k < Gm::kGpt; ++k) raw[k] = st[t + kGroupThreads * k];
 #pragma unroll
       for (int k = 0; k < Gm::kGpt; ++k) group_max<XT>(raw[k], acc);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[sidx]);  // the stage's bytes are all in registers
     }
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, amax_bits(fold_max<XT>(acc)));
-    if (lane == 0) gred[(round & 1) * kGW + gw] = m;
-    named_barrier(1 + grp, kGT);
+    if (lane == 0) gred[(round & 1) * kGroupWarps + gw] = m;
+    named_barrier(1 + grp, kGroupThreads);
     if (!ok) continue;
     uint32_t mb = 0;
 #pragma unroll
-    for (int w = 0; w < kGW; ++w) mb = max(mb, gred[(round & 1) * kGW + w]);
+    for (int w = 0; w < kGroupWarps; ++w) mb = max(mb, gred[(round & 1) * kGroupWarps + w]);
     const float amax = __uint_as_float(mb);
     float sc, r;
     block_scale_of<E5M2>(amax, &sc, &r);
-    const int64_t row0 = (b / nbu) * kBR + t / kGpr, col = (b % nbu) * 128 + (t % kGpr) * kG;
+    const int64_t row0 = (b / nbc) * 128 + t / kGpr, col = (b % nbc) * 128 + (t % kGpr) * kG;
     uint8_t* yp = y + row0 * cols + col;
     const int64_t rows_left = rows - row0;  // this thread's rows k * kRowStep < rows_left exist
     if (col < cols) {
@@ -637,6 +561,67 @@ __global__ __launch_bounds__(BlkGeom<XT, ROWS>::kThreads, 1) void k_fp8_block_tm
       }
     }
     if (t == 0) scales[b] = sc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 1x128 tiles from registers.  Four lanes per tile, each holding a quarter of
+// it (32 elements: 64 B of 16-bit input, 128 B of FP32), one quarter per
+// thread, every CTA the tensor needs launched at once.  At 40 registers six
+// CTAs share an SM, and that occupancy keeps DRAM busier than a TMA-fed ring
+// of 32 x 256 boxes did (16.7 against 19.3 us on [8192 x 4096] BF16; two or
+// four quarters per thread, or eight lanes per tile, were slower; the launch
+// bound holds the 16-bit forms at 40 registers).  The tile
+// max takes two shuffles within the lane quartet; every lane forms the scale
+// (the same value), casts its quarter and stores its 32 output bytes, and the
+// quartet's first lane stores the scale.  Quarter q is part q % 4 of tile
+// q / 4; tile t covers row t / tpr, columns (t % tpr) * 128 .. + 127, with
+// tpr = ceil(cols / 128); past a row's end a partial tile reads zeros, which
+// leave the max unchanged, and stores nothing.
+// ---------------------------------------------------------------------------
+template <int XT, bool E5M2>
+__global__ __launch_bounds__(kThreads, XT == XF32 ? 4 : 6) void k_fp8_rows128(const void* __restrict__ x, int64_t rows, int64_t cols,
+                                                          uint8_t* __restrict__ y, float* __restrict__ scales) {
+  chain_wait();  // the previous kernel in the stream has finished and its writes are visible
+  chain_release();
+  constexpr int kEs = XT == XF32 ? 4 : 2, kG = 16 / kEs, kQG = 32 / kG;  // 16-byte groups per quarter: 4 or 8
+  const int64_t tpr = (cols + 127) / 128, nq = rows * tpr * 4;
+  const int64_t q = (int64_t)blockIdx.x * kThreads + threadIdx.x, t = q >> 2;
+  const int64_t row = t / tpr, col0 = (t % tpr) * 128 + (q & 3) * 32;
+  const bool valid = q < nq;  // whole quartets: nq is a multiple of 4
+  const unsigned char* xr = static_cast<const unsigned char*>(x) + row * cols * kEs;
+  uint4 raw[kQG];
+#pragma unroll
+  for (int k = 0; k < kQG; ++k) {
+    const int64_t c = col0 + k * kG;
+    raw[k] = (valid && c < cols) ? __ldcs(reinterpret_cast<const uint4*>(xr + c * kEs)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+  uint32_t acc[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int k = 0; k < kQG; ++k) group_max<XT>(raw[k], acc);
+  uint32_t m = amax_bits(fold_max<XT>(acc));  // ordered bits, NaN above inf
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  float sc, r;
+  block_scale_of<E5M2>(__uint_as_float(m), &sc, &r);
+  if (!valid) return;
+  if ((q & 3) == 0) scales[row * tpr + col0 / 128] = sc;
+  uint8_t* yp = y + row * cols + col0;
+  constexpr int kPer = 16 / kG;  // groups per 16 output bytes
+#pragma unroll
+  for (int k = 0; k < kQG; k += kPer) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const uint2 o = r > 0.0f ? cast_group_finite<XT, E5M2>(raw[k + j], r) : cast_group<XT, E5M2>(raw[k + j], r);
+      if constexpr (XT == XF32) {
+        w[j] = o.x;
+      } else {
+        w[2 * j] = o.x;
+        w[2 * j + 1] = o.y;
+      }
+    }
+    if (col0 + k * kG < cols) st_cs(yp + k * kG, make_uint4(w[0], w[1], w[2], w[3]));  // cols % 16 == 0
   }
 }
 
@@ -842,23 +827,19 @@ mp_status launch_t(const void* x, int64_t rows, int64_t cols, uint8_t* y, uint8_
 template <int XT, bool E5M2>
 mp_status launch_blockwise(const void* x, int64_t rows, int64_t cols, bool square, uint8_t* y, float* scales,
                            cudaStream_t s) {
-  CUtensorMap map;
   if (square) {
-    using Gm = BlkGeom<XT, false>;
-    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, Gm::kBoxCols)) return MP_ECUDA;
-    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + Gm::kBoxCols - 1) / Gm::kBoxCols);
+    using Gm = BlkGeom<XT>;
+    CUtensorMap map;
+    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, 128, 128)) return MP_ECUDA;
+    const int64_t boxes = ((rows + 127) / 128) * ((cols + 127) / 128);
     static std::atomic<uint64_t> smem_done{0};
-    if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, false>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
-    launch_chained(k_fp8_block_tma<XT, E5M2, false>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
+    if (!smem_opt_in(k_fp8_block_tma<XT, E5M2>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
+    launch_chained(k_fp8_block_tma<XT, E5M2>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
                    rows, cols, y, scales);
   } else {
-    using Gm = BlkGeom<XT, true>;
-    if (!encode_tile_map_2d(&map, x, Gm::kEs, rows, cols, Gm::kBoxRows, Gm::kBoxCols)) return MP_ECUDA;
-    const int64_t boxes = ((rows + Gm::kBoxRows - 1) / Gm::kBoxRows) * ((cols + Gm::kBoxCols - 1) / Gm::kBoxCols);
-    static std::atomic<uint64_t> smem_done{0};
-    if (!smem_opt_in(k_fp8_block_tma<XT, E5M2, true>, (int)Gm::kSmem, smem_done)) return MP_ECUDA;
-    launch_chained(k_fp8_block_tma<XT, E5M2, true>, dim3(grid_for(boxes, 1)), dim3(Gm::kThreads), Gm::kSmem, s, map,
-                   rows, cols, y, scales);
+    const int64_t quarters = rows * ((cols + 127) / 128) * 4;
+    launch_chained(k_fp8_rows128<XT, E5M2>, dim3(full_grid((quarters + kThreads - 1) / kThreads)), dim3(kThreads), 0,
+                   s, x, rows, cols, y, scales);
   }
   note_launches(1);
   return launch_status();
